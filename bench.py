@@ -1,0 +1,447 @@
+"""Benchmark of one paged-decode step: cache write + PagedAttention decode.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3_8b|long_ctx|mixed_prefix|gqa8_70b|gqa8_70b_bs32|tiny_fp32]
+
+A step is one pass of the whole hot path over one seeded synthetic batch:
+pa_write_cache (each sequence's newest token into the pool) then pa_decode.
+The default workload is the Llama-3-8B-shaped batch (64 sequences, 32/8 heads,
+head 128, block 16, contexts uniform in [512, 4096], bf16).  Its valid K/V
+(~0.6 GB) is larger than L2, so no flush is needed between steps.
+
+Output: one JSON line (rank 0).  `value` is effective GB/s = algorithmic bytes
+of the step (K+V over the valid contexts, q, out, the valid block-table
+entries, context lengths, the write's rows and slots) / device time.
+Under torchrun with N>1 every rank runs an independent replica (no collective
+on the data path); the max time over ranks is used and `value` sums all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_kv_cache_292_gb300 import workloads  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_292_gb300", "csrc", "pa_decode.cu")
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+WORKLOADS = {
+    "llama3_8b": ("llama3_8b", None),
+    "long_ctx": ("long_ctx", None),
+    "mixed_prefix": ("mixed_prefix", None),
+    "gqa8_70b": ("gqa8_70b", 16),
+    "gqa8_70b_bs32": ("gqa8_70b", 32),
+    "tiny_fp32": ("tiny_fp32", None),
+}
+
+
+def step_bytes(w) -> dict:
+    """Algorithmic bytes of one step (nothing that a perfect kernel could avoid)."""
+    sp = w.spec
+    e = 4 if sp.dtype == "f32" else 2
+    ctx = w.context_lens.numpy().astype(np.int64)
+    nblk = -(-ctx // sp.block_size)
+    kv = int(ctx.sum()) * 2 * sp.num_kv_heads * sp.head_size * e
+    qo = 2 * sp.num_seqs * sp.num_heads * sp.head_size * e
+    tables = 4 * int(nblk.sum()) + 4 * sp.num_seqs
+    decode = kv + qo + tables
+    wr_tokens = int((w.slot_mapping.numpy() >= 0).sum())
+    write = 2 * 2 * wr_tokens * sp.num_kv_heads * sp.head_size * e + 8 * sp.num_seqs
+    # Unique physical K/V actually resident (prefix blocks counted once).
+    return {"decode": decode, "write": write, "step": decode + write, "kv_logical": kv}
+
+
+def read_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def read_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    or None if missing or taken on a different kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        rec = t.get(workload)
+        if rec and rec.get("kernel_sha") == kernel_hash():
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [[c.strip() for c in line.split(",")] for line in out.strip().splitlines() if line.strip()]
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons),
+            "samples": len(sm),
+        }
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def make_replica(name: str, rank: int):
+    spec_name, bs = WORKLOADS[name]
+    sp = workloads.spec(spec_name)
+    if rank:
+        sp = workloads.dataclasses.replace(sp, seed=sp.seed + 1000 * rank)
+    return workloads.make_workload(sp, block_size=bs, prewritten=False)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reported baseline only)
+# ---------------------------------------------------------------------------
+
+
+def time_oracle(w, budget_s: float, max_seqs: int = None):
+    """Run the fp64 oracle (as it stands) on a bounded sample of the batch:
+    the cache write of the sampled sequences' new tokens, then their decode.
+    Returns (seconds, bytes of that sample, description)."""
+    import oracle
+
+    sp = w.spec
+    e = 4 if sp.dtype == "f32" else 2
+    bs = sp.block_size
+    order = list(range(sp.num_seqs))
+    ctx_all = w.context_lens.numpy().astype(np.int64)
+    done, secs, nbytes = 0, 0.0, 0
+    for s in order:
+        if max_seqs is not None and done >= max_seqs:
+            break
+        if secs >= budget_s and done > 0:
+            break
+        c = int(ctx_all[s])
+        n = -(-c // bs)
+        ids = w.block_tables[s, :n].long()
+        # Compact this sequence's blocks (plumbing, not timed).
+        view = torch.int32 if sp.dtype == "f32" else torch.int16
+        kc = w.k_cache[ids].view(view).numpy()
+        vc = w.v_cache[ids].view(view).numpy()
+        slot = int(w.slot_mapping[s])
+        local_slot = (n - 1) * bs + slot % bs
+        bt = np.arange(n)[None, :]
+        q = w.q[s : s + 1].double().numpy()
+        kn = w.k_new[s : s + 1].view(view).numpy()
+        vn = w.v_new[s : s + 1].view(view).numpy()
+        t0 = time.perf_counter()
+        k2, v2 = oracle.write_cache(kc, vc, kn, vn, np.array([local_slot]), bs)
+        k64 = torch.from_numpy(k2).view(w.k_cache.dtype).double().numpy()
+        v64 = torch.from_numpy(v2).view(w.v_cache.dtype).double().numpy()
+        oracle.decode(q, k64, v64, bt, np.array([c]), w.scale, bs)
+        secs += time.perf_counter() - t0
+        nbytes += c * 2 * sp.num_kv_heads * sp.head_size * e + 2 * sp.num_heads * sp.head_size * e + 4 * n + 4
+        nbytes += 2 * 2 * sp.num_kv_heads * sp.head_size * e + 8
+        done += 1
+    desc = f"{done} of {sp.num_seqs} sequences (write + decode), fp64 NumPy oracle"
+    return secs, nbytes, desc
+
+
+def cpu_threads() -> int:
+    try:
+        import threadpoolctl  # noqa: F401
+
+        from threadpoolctl import threadpool_info
+
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    w = make_replica(args.workload, 0)
+    by = step_bytes(w)
+    per_step_budget = 20.0 / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        time_oracle(w, per_step_budget)
+    secs, nbytes = 0.0, 0
+    for _ in range(args.steps):
+        s, b, desc = time_oracle(w, per_step_budget)
+        secs += s
+        nbytes += b
+    gbs = nbytes / secs / 1e9
+    ms = secs / args.steps * 1e3
+    line = {
+        "impl": "reference",
+        "metric": "paged decode attention: effective KV GB/s (% of GB300 HBM peak), us/step",
+        "value": gbs, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), PCG64)",
+        "config": {"workload": args.workload, "sample": desc, "full_step_bytes": by["step"]},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+
+def run_ours(args):
+    from paged_kv_cache_292_gb300 import binding
+    from paged_kv_cache_292_gb300 import build as pa_build
+
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    pa_build.build()
+    lib = binding.load()
+
+    w = make_replica(args.workload, rank)
+    sp = w.spec
+    by = step_bytes(w)
+    S, H, D = w.q.shape
+    Hk, bs, NB, MB = sp.num_kv_heads, sp.block_size, w.num_blocks, w.max_blocks_per_seq
+    dt = binding.dtype_code(w.q.dtype)
+    g = {k: getattr(w, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_tables", "context_lens",
+                                             "slot_mapping", "k_new", "v_new")}
+    out = torch.empty_like(g["q"])
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    ws_bytes = lib.pa_decode_workspace_size(S, H, Hk, D, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    P = binding._ptr
+
+    def write(gg):
+        rc = lib.pa_write_cache(P(gg["k_new"]), P(gg["v_new"]), P(gg["slot_mapping"]), P(g["k_cache"]),
+                                P(g["v_cache"]), S, Hk, D, bs, NB, sh, dt)
+        if rc:
+            raise RuntimeError(binding.pa_last_error())
+
+    def decode(gg, o):
+        rc = lib.pa_decode_ws(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
+                              P(gg["context_lens"]), S, H, Hk, D, bs, MB, w.scale, sh, dt, P(ws), ws_bytes)
+        if rc:
+            raise RuntimeError(binding.pa_last_error())
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- device-resident timing ----
+    for _ in range(args.warmup):
+        write(g)
+        decode(g, out)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(args.steps):
+        write(g)
+        ev[i][0].record(stream)
+        decode(g, out)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * by["step"] / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API, host buffers ----
+    host = {k: getattr(w, k).pin_memory() for k in ("q", "block_tables", "context_lens", "slot_mapping", "k_new",
+                                                    "v_new")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d2h = out_host.numel() * out_host.element_size()
+    dev_in = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    e2e_steps = max(10, min(args.steps, 1000))
+
+    def e2e_step():
+        for k, t in host.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        write(dev_in)
+        decode(dev_in, out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * by["step"] / (e2e_ms * 1e-3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak, peak_kind = read_peaks()
+    achieved = by["decode"] / (dec_ms * 1e-3) / 1e9
+    traffic = read_traffic(args.workload)
+    line = {
+        "metric": "paged decode attention: effective KV GB/s (% of GB300 HBM peak), us/step",
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "us_per_step": ms_step * 1e3,
+        "pct_of_hbm_peak": 100.0 * value / world / peak,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if sp.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) K/V/q via PCG64, cast RNE to bf16; shuffled block pool)",
+        "config": {
+            "workload": args.workload,
+            "num_seqs": S, "num_heads": H, "num_kv_heads": Hk, "head_size": D, "block_size": bs,
+            "num_physical_blocks": NB, "context_tokens": int(w.context_lens.sum()),
+            "step_bytes": by["step"], "decode_bytes": by["decode"], "write_bytes": by["write"],
+            "l2": f"inputs larger than L2: {by['kv_logical'] / 1e9:.3f} GB of K/V read per step vs "
+                  f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
+            "replicas": world,
+        },
+        "roofline": {
+            "kernel": "pa_decode (decode kernel + LSE merge kernel, one C-ABI call)",
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "decode_us": dec_ms * 1e3,
+        },
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms,
+                "note": "per-step inputs (q, new K/V, slots, tables, lengths) from pinned host, output back; "
+                        "the paged pool is device-resident state"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if args.cpu_baseline:
+        secs, nbytes, desc = time_oracle(w, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cpu_threads(),
+                                "kind": "oracle", "sample": desc, "seconds": secs}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="llama3_8b")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+/*
+ * pagedattn.h - C ABI of the GB300 (sm_103a) paged decode-attention library.
+ *
+ * The operation is the PagedAttention decode step described in "vLLM
+ * three-process architecture and the PagedAttention kernel" (devpress.csdn.net),
+ * section 3 "PagedAttention 内核原理：从概念到 CUDA 实现":
+ *   3.1 "输入是什么": query[num_seqs, num_heads, head_size],
+ *       block_tables[num_seqs, max_blocks_per_seq],
+ *       k_cache / v_cache[num_physical_blocks, block_size, num_kv_heads, head_size];
+ *   3.2 "内核执行流程（简化版）": for each sequence, read its block table (step 1),
+ *       derive the number of logical blocks from its valid length (step 2),
+ *       gather K/V from the scattered physical blocks (step 3), run standard
+ *       attention with the step's query (step 4), write the output (step 5).
+ * Section 2 "工作流程拆解", item 4, appends each new token's K/V into the
+ * sequence's current physical block: pa_write_cache.
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is DEVICE memory owned by the caller, dense and
+ *     row-major in the shape given.  The library never frees or keeps it.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on that stream and never synchronise the host.
+ *   - The return value is PA_OK (0) or a negative PA_ERR_* code; on error
+ *     nothing was launched and pa_last_error() describes the cause.
+ *   - `dtype` is PA_F32 or PA_BF16 and applies to query, out, the pools and
+ *     the new K/V rows alike.  Arithmetic is fp32 in every case.
+ *   - Query head h reads KV head h / (num_heads / num_kv_heads).
+ *   - context_lens[s] counts every valid token of sequence s, including the
+ *     current step's (written by pa_write_cache first).  Token t of sequence s
+ *     is row t % block_size of physical block block_tables[s][t / block_size].
+ *     Table entries at or past ceil(context_lens[s] / block_size), and pool rows
+ *     no valid token occupies, are never read.  context_lens[s] == 0 gives an
+ *     all-zero output row.
+ *   - Device-detected input faults (a block id outside [0, num_physical_blocks),
+ *     a context length beyond max_blocks_per_seq * block_size or negative, a
+ *     slot outside the pool) are reported by OR-ing PA_DEVERR_* bits into the
+ *     optional device word `error_flag`; the offending row is skipped (its
+ *     content is then unspecified) instead of being read or written.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG (-1) /* null pointer, bad size, misaligned pointer */
+#define PA_ERR_UNSUPPORTED (-2) /* valid but not built: head_size, group size, dtype */
+#define PA_ERR_CUDA (-3)        /* a CUDA runtime call failed (message kept) */
+#define PA_ERR_WORKSPACE (-4)   /* caller workspace smaller than required */
+
+/* Element types. */
+#define PA_F32 0
+#define PA_BF16 1
+
+/* Bits OR-ed into the optional device error word. */
+#define PA_DEVERR_BLOCK_ID 1    /* block id outside [0, num_physical_blocks) */
+#define PA_DEVERR_CONTEXT_LEN 2 /* context length < 0 or > max_blocks_per_seq*block_size (clamped) */
+#define PA_DEVERR_SLOT 4        /* slot_mapping entry >= num_physical_blocks*block_size (skipped) */
+#define PA_DEVERR_TIMEOUT 8     /* a pipeline wait exceeded its limit; the kernel returned early */
+
+/*
+ * pa_decode - paged decode attention, one query token per sequence.
+ *
+ *   out[s, h, :] = sum_t softmax_t(scale * <query[s, h, :], K_s[t, h/G, :]>) V_s[t, h/G, :]
+ *
+ * out          [num_seqs, num_heads, head_size], dtype            (written)
+ * query        [num_seqs, num_heads, head_size], dtype
+ * k_cache      [num_physical_blocks, block_size, num_kv_heads, head_size], dtype
+ * v_cache      same shape as k_cache
+ * block_tables [num_seqs, max_blocks_per_seq] int32
+ * context_lens [num_seqs] int32
+ * Requirements: num_heads % num_kv_heads == 0 and num_heads / num_kv_heads <= 8;
+ * head_size 64 or 128; block_size in [1, 4096]; query, out and both pools
+ * 16-byte aligned.
+ * Long sequences are split across CTAs and their partial softmax statistics
+ * merged by a second log-sum-exp kernel; the scratch for that comes from a
+ * per-device buffer the library allocates on first use and grows when a
+ * larger batch needs it (cudaMalloc, which synchronises the device; use
+ * pa_decode_ws to supply the scratch and never allocate).
+ */
+int pa_decode(void* out, const void* query, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+              int num_heads, int num_kv_heads, int head_size, int block_size,
+              int max_blocks_per_seq, float scale, void* stream, int dtype);
+
+/*
+ * pa_decode_workspace_size - bytes of scratch pa_decode_ws needs on the
+ * current device for this batch shape (num_ranges as in pa_decode_ex; 0 =
+ * the default of one range per SM).  Returns 0 for invalid sizes.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                int num_ranges);
+
+/*
+ * pa_decode_ws - pa_decode with caller-owned scratch (device memory of at
+ * least pa_decode_workspace_size(...) bytes, 256-byte aligned).  Never
+ * allocates.  The scratch may be reused by the next call on the same stream;
+ * two calls that overlap in time must not share it.
+ */
+int pa_decode_ws(void* out, const void* query, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                 int num_heads, int num_kv_heads, int head_size, int block_size,
+                 int max_blocks_per_seq, float scale, void* stream, int dtype, void* workspace,
+                 size_t workspace_bytes);
+
+/*
+ * pa_decode_ex - the general form behind pa_decode and pa_decode_ws.
+ *
+ * num_physical_blocks  > 0: every block id read from block_tables is checked
+ *                      against it on the device (PA_DEVERR_BLOCK_ID); 0: unchecked.
+ * workspace            NULL: library-owned scratch (may allocate, see pa_decode).
+ * num_ranges           0: one token range per SM (the default).  > 0: split the
+ *                      flattened batch into exactly this many ranges (1 = a
+ *                      single CTA walks every sequence in one pass).
+ * error_flag           optional device int32 that receives PA_DEVERR_* bits.
+ */
+int pa_decode_ex(void* out, const void* query, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                 int num_heads, int num_kv_heads, int head_size, int block_size,
+                 int max_blocks_per_seq, float scale, void* stream, int dtype,
+                 int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                 int32_t* error_flag);
+
+/*
+ * pa_write_cache - scatter one step's new K/V rows into the paged pool
+ * (the "reshape_and_cache" step).  For every token i with slot_mapping[i] >= 0:
+ *   k_cache[slot / block_size, slot % block_size, :, :] = k_new[i, :, :]  (bit copy)
+ * and the same for V.  Negative slots are padding and are skipped; slots at
+ * or beyond num_physical_blocks * block_size are skipped and reported.
+ * Duplicate slots within one call leave either row (unspecified which).
+ * k_new, v_new  [num_tokens, num_kv_heads, head_size], dtype, 16-byte aligned
+ * slot_mapping  [num_tokens] int64
+ * k_cache, v_cache as in pa_decode (written in place).
+ */
+int pa_write_cache(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                   void* k_cache, void* v_cache, int num_tokens, int num_kv_heads, int head_size,
+                   int block_size, int num_physical_blocks, void* stream, int dtype);
+
+/* pa_write_cache_ex - pa_write_cache with an optional device error word. */
+int pa_write_cache_ex(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                      void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
+                      int head_size, int block_size, int num_physical_blocks, void* stream,
+                      int dtype, int32_t* error_flag);
+
+/* Message for the calling thread's last non-zero return ("" if none). */
+const char* pa_last_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

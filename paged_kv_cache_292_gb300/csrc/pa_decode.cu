@@ -1,0 +1,928 @@
+// Paged decode attention for sm_103a.
+//
+// What it computes is section 3.2 ("内核执行流程（简化版）") of "vLLM
+// three-process architecture and the PagedAttention kernel": for each
+// sequence, look up its block table (step 1), bound the walk by its valid
+// length (step 2), gather K/V from the scattered physical blocks (step 3),
+// attend with the step's query (step 4) and write the output (step 5).  The
+// same section's "精妙之处" asks for the gather to be planned up front and for
+// copies to overlap compute on the GPU's separate copy engine; here that is a
+// producer warp driving the TMA engine's bulk copies into a ring of shared-
+// memory stages while consumer warps compute on earlier stages.
+//
+// Kernel 1 (pa_decode_kernel), one CTA per (token range, KV-head group):
+//   * The flattened tile list of the batch is cut into equal ranges (see
+//     pa_schedule.h), so every CTA moves the same K/V bytes.
+//   * Warp `Hg` (the producer) walks the range tile by tile.  For each tile of
+//     16 tokens it looks up the block ids, then issues one bulk copy per token
+//     row of K and of V: a row is all `Hg` KV heads of the token, contiguous in
+//     the pool ([block, slot, head, dim] layout), e.g. 2 KiB for 8 heads x 128
+//     x bf16.  Rows land `pitch = row + 16` bytes apart so that ldmatrix reads
+//     of 8 consecutive tokens hit distinct banks.  Each sequence's query slice
+//     is copied once into a small ring of its own.
+//   * Warp w < Hg (a consumer) owns KV head w and its G query heads.  bf16:
+//     S^T[16 tok x 8] = K_tile[16 x D] * Q^T[D x 8] on the tensor cores
+//     (mma.sync m16n8k16, query heads padded to 8), online softmax in
+//     registers (running max and sum in the exp2 domain), then
+//     O^T[D x 8] += V^T[D x 16] * P^T[16 x 8], with P^T obtained from the score
+//     fragment by movmatrix.  fp32: the same on CUDA cores.
+//   * A sequence wholly inside the range is written to `out` directly; a
+//     sequence cut by the range boundary leaves (m, l, O) partials.
+// Kernel 2 (pa_merge_kernel), one CTA per sequence: merges the partials of cut
+// sequences by log-sum-exp and zero-fills empty sequences.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <float.h>
+#include <math.h>
+
+#include <cmath>
+#include <type_traits>
+
+#include "../../include/pagedattn.h"
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_schedule.h"
+
+namespace pa {
+
+constexpr int kMaxGroupHeads = 8;  // KV heads per CTA (one consumer warp each)
+constexpr int kMaxQueryGroup = 8;  // query heads per KV head (MMA N extent)
+constexpr int kRowSkew = 16;       // bytes between staged rows beyond the row itself
+constexpr int kMaxStages = 6;
+
+enum : int { kSegBegin = 1, kSegEnd = 2 };
+
+struct StageMeta {
+  int seq;     // sequence index
+  int tok0;    // first token of the tile within the sequence
+  int nvalid;  // valid tokens in the tile (1..16)
+  int flags;   // kSegBegin | kSegEnd | (output slot + 1) << 2
+};
+
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t* prefix;  // [num_seqs + 1] tile offsets (written by range 0's CTAs)
+  float* part_ml;   // [R][2][H][2]: (m in log2 units, l)
+  float* part_o;    // [R][2][H][D]: un-normalised weighted V sums
+  int32_t* error_flag;
+  int num_seqs, num_heads, num_kv_heads, group, block_size, max_blocks_per_seq;
+  int heads_per_cta;    // Hg
+  int num_head_groups;  // HG = Hk / Hg
+  int num_ranges;       // R
+  int num_physical_blocks;
+  int stages, q_slots;
+  uint32_t row_bytes, pitch, q_bytes, stage_bytes;
+  float scale_log2;  // scale * log2(e)
+};
+
+struct Layout {
+  uint32_t bar, meta, misc, qring, stage, total;
+};
+
+// Shared-memory carve-up; identical on host (sizing) and device (addressing).
+PA_HD Layout make_layout(int stages, int q_slots, uint32_t q_bytes, uint32_t stage_bytes) {
+  Layout L;
+  uint32_t o = 0;
+  L.bar = o;
+  o += 8u * (2u * stages + 2u * q_slots);
+  o = (o + 15u) & ~15u;
+  L.meta = o;
+  o += 16u * stages;
+  L.misc = o;
+  o += 4u * 80u;
+  o = (o + 127u) & ~127u;
+  L.qring = o;
+  o += q_slots * ((q_bytes + 127u) & ~127u);
+  o = (o + 127u) & ~127u;
+  L.stage = o;
+  o += stages * stage_bytes;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ int clamp_context(const DecodeParams& p, int s, bool report_it) {
+  int c = __ldg(p.context_lens + s);
+  const int cmax = p.max_blocks_per_seq * p.block_size;
+  if (c < 0 || c > cmax) {
+    if (report_it) report(p.error_flag, PA_DEVERR_CONTEXT_LEN);
+    c = c < 0 ? 0 : cmax;
+  }
+  return c;
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ long long warp_incl_scan_ll(long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Consumer state and tile math.  One consumer warp = one KV head and its G
+// query heads; D = head size.
+// ---------------------------------------------------------------------------
+
+// bf16 tensor-core consumer.  Lane l owns query heads hA = 2*(l%4), hB = hA+1
+// (columns of the score fragment) and, per 16-wide slice mt of the head
+// dimension, output dims mt*16 + l/4 and +8.
+template <int D>
+struct MmaConsumer {
+  static constexpr int KS = D / 16;  // k-steps of Q.K and m-tiles of P.V
+  uint32_t qb[KS][2];
+  float acc[KS][4];
+  float m_a, m_b, l_a, l_b;
+
+  __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G,
+                                                int lane) {
+    const int n = lane >> 2, t2 = 2 * (lane & 3);
+    const __nv_bfloat16* qh =
+        reinterpret_cast<const __nv_bfloat16*>(qslot) + (size_t)(w * G + n) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (n < G) {
+        qb[ks][0] = *reinterpret_cast<const uint32_t*>(qh + ks * 16 + t2);
+        qb[ks][1] = *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + t2);
+      } else {
+        qb[ks][0] = 0u;
+        qb[ks][1] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[ks][i] = 0.f;
+    }
+    m_a = m_b = -INFINITY;
+    l_a = l_b = 0.f;
+  }
+
+  __device__ __forceinline__ void tile(uint32_t k_base, uint32_t v_base, uint32_t pitch,
+                                       int nvalid, float scale_log2, int lane) {
+    // S^T = K_tile * Q^T : rows = tokens, columns = query heads.
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t k_lane = k_base + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 16;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      ldmatrix_x4(a, k_lane + ks * 32);
+      if (ks & 1)
+        mma_bf16_16816(c1, a, qb[ks][0], qb[ks][1]);
+      else
+        mma_bf16_16816(c0, a, qb[ks][0], qb[ks][1]);
+    }
+    const int r0 = lane >> 2;
+    float s0 = (c0[0] + c1[0]) * scale_log2, s1 = (c0[1] + c1[1]) * scale_log2;
+    float s2 = (c0[2] + c1[2]) * scale_log2, s3 = (c0[3] + c1[3]) * scale_log2;
+    if (r0 >= nvalid) s0 = s1 = -INFINITY;
+    if (r0 + 8 >= nvalid) s2 = s3 = -INFINITY;
+
+    // Online softmax: per-head tile maximum across the 8 lanes sharing l%4.
+    float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, o));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, o));
+    }
+    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+    // A tile always holds a valid token, so mn_* is finite unless the inputs
+    // are not; guard the exponent base anyway so -inf - -inf never appears.
+    const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
+    const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
+    const float alpha_a = exp2f(m_a - base_a), alpha_b = exp2f(m_b - base_b);
+    m_a = mn_a;
+    m_b = mn_b;
+    const uint32_t p_top = pack_bf16x2(exp2f(s0 - base_a), exp2f(s1 - base_b));
+    const uint32_t p_bot = pack_bf16x2(exp2f(s2 - base_a), exp2f(s3 - base_b));
+    // The sum uses the rounded weights the P.V product sees.
+    l_a = l_a * alpha_a + bf16_lo(p_top) + bf16_lo(p_bot);
+    l_b = l_b * alpha_b + bf16_hi(p_top) + bf16_hi(p_bot);
+    const uint32_t pb0 = movmatrix_trans(p_top);  // P^T rows (tokens) 0-7
+    const uint32_t pb1 = movmatrix_trans(p_bot);  // tokens 8-15
+
+    // O^T += V^T * P^T : rows = head dims, columns = query heads.
+    const uint32_t v_lane = v_base + ((lane & 7) + (lane >> 4) * 8) * pitch + ((lane >> 3) & 1) * 16;
+    const int t2 = 2 * (lane & 3);
+    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+    if (nvalid < kTile) {
+      // Zero V entries of tokens past the end so stale stage contents (which
+      // may be non-finite) never meet a zero weight.
+      keep_lo = (t2 < nvalid ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid ? 0xffff0000u : 0u);
+      keep_hi = (t2 + 8 < nvalid ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, v_lane + mt * 32);
+      a[0] &= keep_lo;
+      a[1] &= keep_lo;
+      a[2] &= keep_hi;
+      a[3] &= keep_hi;
+      acc[mt][0] *= alpha_a;
+      acc[mt][1] *= alpha_b;
+      acc[mt][2] *= alpha_a;
+      acc[mt][3] *= alpha_b;
+      mma_bf16_16816(acc[mt], a, pb0, pb1);
+    }
+  }
+
+  // slot < 0: final output; else partial slot of range r.
+  __device__ __forceinline__ void finish(const DecodeParams& p, int seq, int kv_head, int slot,
+                                         int r, int lane) {
+    float la = l_a, lb = l_b;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      la += __shfl_xor_sync(0xffffffffu, la, o);
+      lb += __shfl_xor_sync(0xffffffffu, lb, o);
+    }
+    const int G = p.group, H = p.num_heads;
+    const int ha = 2 * (lane & 3), hb = ha + 1, d0 = lane >> 2;
+    const int qa = kv_head * G + ha, qb_ = kv_head * G + hb;
+    if (slot < 0) {
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)seq * H * D;
+      const float ia = 1.f / la, ib = 1.f / lb;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int d = mt * 16 + d0;
+        if (ha < G) {
+          out[(size_t)qa * D + d] = __float2bfloat16_rn(acc[mt][0] * ia);
+          out[(size_t)qa * D + d + 8] = __float2bfloat16_rn(acc[mt][2] * ia);
+        }
+        if (hb < G) {
+          out[(size_t)qb_ * D + d] = __float2bfloat16_rn(acc[mt][1] * ib);
+          out[(size_t)qb_ * D + d + 8] = __float2bfloat16_rn(acc[mt][3] * ib);
+        }
+      }
+    } else {
+      const size_t base = ((size_t)r * 2 + slot) * H;
+      float* po = p.part_o + base * D;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int d = mt * 16 + d0;
+        if (ha < G) {
+          po[(size_t)qa * D + d] = acc[mt][0];
+          po[(size_t)qa * D + d + 8] = acc[mt][2];
+        }
+        if (hb < G) {
+          po[(size_t)qb_ * D + d] = acc[mt][1];
+          po[(size_t)qb_ * D + d + 8] = acc[mt][3];
+        }
+      }
+      if (d0 == 0) {
+        float* pm = p.part_ml + base * 2;
+        if (ha < G) {
+          pm[(size_t)qa * 2 + 0] = m_a;
+          pm[(size_t)qa * 2 + 1] = la;
+        }
+        if (hb < G) {
+          pm[(size_t)qb_ * 2 + 0] = m_b;
+          pm[(size_t)qb_ * 2 + 1] = lb;
+        }
+      }
+    }
+  }
+};
+
+// fp32 CUDA-core consumer.  Lane l owns head dims [l*DC, l*DC+DC) of every
+// query head; after the butterfly reduction lane l holds the score of token l/2.
+template <int D, int GMAX>
+struct SimtConsumer {
+  static constexpr int DC = D / 32;
+  float qv[GMAX][DC];
+  float acc[GMAX][DC];
+  float m[GMAX], l[GMAX];  // l: this lane's share (token l/2, counted on even and odd lanes)
+
+  __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G,
+                                                int lane) {
+    const float* qh = reinterpret_cast<const float*>(qslot) + (size_t)w * G * D;
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+#pragma unroll
+      for (int i = 0; i < DC; ++i) {
+        qv[h][i] = (h < G) ? qh[(size_t)h * D + lane * DC + i] : 0.f;
+        acc[h][i] = 0.f;
+      }
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void tile(const unsigned char* k_base, const unsigned char* v_base,
+                                       uint32_t pitch, int nvalid, float scale_log2, int G,
+                                       int lane) {
+    const int my_tok = lane >> 1;
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      if (h >= G) break;
+      float part[kTile];
+#pragma unroll
+      for (int t = 0; t < kTile; ++t) {
+        const float* kr = reinterpret_cast<const float*>(k_base + t * pitch) + lane * DC;
+        float sacc = 0.f;
+#pragma unroll
+        for (int i = 0; i < DC; ++i) sacc = fmaf(qv[h][i], kr[i], sacc);
+        part[t] = sacc;
+      }
+      // Butterfly reduce-scatter: 16 partial sums over 32 lanes -> one full sum
+      // per lane pair.  Step xor 16 keeps the half selected by lane bit 4, etc.
+      float v8[8], v4[4], v2[2];
+      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float mine = b4 ? part[i + 8] : part[i];
+        const float give = b4 ? part[i] : part[i + 8];
+        v8[i] = mine + __shfl_xor_sync(0xffffffffu, give, 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float mine = b3 ? v8[i + 4] : v8[i];
+        const float give = b3 ? v8[i] : v8[i + 4];
+        v4[i] = mine + __shfl_xor_sync(0xffffffffu, give, 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float mine = b2 ? v4[i + 2] : v4[i];
+        const float give = b2 ? v4[i] : v4[i + 2];
+        v2[i] = mine + __shfl_xor_sync(0xffffffffu, give, 4);
+      }
+      float sc;
+      {
+        const float mine = b1 ? v2[1] : v2[0];
+        const float give = b1 ? v2[0] : v2[1];
+        sc = mine + __shfl_xor_sync(0xffffffffu, give, 2);
+      }
+      sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+      sc *= scale_log2;
+      if (my_tok >= nvalid) sc = -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float mn = fmaxf(m[h], mx);
+      const float base = (mn == -INFINITY) ? 0.f : mn;
+      const float alpha = exp2f(m[h] - base);
+      m[h] = mn;
+      const float pw = exp2f(sc - base);
+      l[h] = l[h] * alpha + pw;
+#pragma unroll
+      for (int i = 0; i < DC; ++i) acc[h][i] *= alpha;
+      for (int t = 0; t < nvalid; ++t) {
+        const float pt = __shfl_sync(0xffffffffu, pw, 2 * t);
+        const float* vr = reinterpret_cast<const float*>(v_base + t * pitch) + lane * DC;
+#pragma unroll
+        for (int i = 0; i < DC; ++i) acc[h][i] = fmaf(pt, vr[i], acc[h][i]);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void finish(const DecodeParams& p, int seq, int kv_head, int slot,
+                                         int r, int lane) {
+    const int G = p.group, H = p.num_heads;
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      if (h >= G) break;
+      float lt = l[h];
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+      const int qh = kv_head * G + h;
+      if (slot < 0) {
+        float* out = reinterpret_cast<float*>(p.out) + ((size_t)seq * H + qh) * D + lane * DC;
+        const float inv = 1.f / lt;
+#pragma unroll
+        for (int i = 0; i < DC; ++i) out[i] = acc[h][i] * inv;
+      } else {
+        const size_t base = ((size_t)r * 2 + slot) * H + qh;
+        float* po = p.part_o + base * D + lane * DC;
+#pragma unroll
+        for (int i = 0; i < DC; ++i) po[i] = acc[h][i];
+        if (lane == 0) {
+          p.part_ml[base * 2 + 0] = m[h];
+          p.part_ml[base * 2 + 1] = lt;
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Kernel 1
+// ---------------------------------------------------------------------------
+template <typename T, int D, int GMAX>
+__global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
+    pa_decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int HG = p.num_head_groups, R = p.num_ranges, S = p.num_seqs;
+  const int r = blockIdx.x / HG, hg = blockIdx.x % HG;
+  const int Hg = p.heads_per_cta;
+  const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes);
+  long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
+  const bool write_prefix = (r == 0 && hg == 0);
+
+  // ---- Prologue: total tile count, this range, and its first sequence. ----
+  long long total = 0;
+  for (int base = 0; base < S; base += nthreads) {
+    const int s = base + tid;
+    long long n = (s < S) ? tiles_of(clamp_context(p, s, true)) : 0;
+    n = warp_sum_ll(n);
+    if (lane == 0) misc[warp] = n;
+    __syncthreads();
+    for (int w = 0; w < nwarps; ++w) total += misc[w];
+    __syncthreads();
+  }
+  const long long a = range_start(r, total, R), b = range_start(r + 1, total, R);
+  if (a == b && !write_prefix) return;
+
+  long long run = 0;
+  for (int base = 0; base < S; base += nthreads) {
+    const int s = base + tid;
+    const long long n = (s < S) ? tiles_of(clamp_context(p, s, false)) : 0;
+    const long long incl = warp_incl_scan_ll(n, lane);
+    if (lane == 31) misc[warp] = incl;
+    __syncthreads();
+    long long before = run;
+    for (int w = 0; w < warp; ++w) before += misc[w];
+    long long chunk = 0;
+    for (int w = 0; w < nwarps; ++w) chunk += misc[w];
+    const long long excl = before + incl - n;
+    if (s < S) {
+      if (write_prefix) p.prefix[s] = static_cast<int32_t>(excl);
+      if (n > 0 && excl <= a && a < excl + n) {
+        misc[32] = s;
+        misc[33] = excl;
+      }
+    }
+    run += chunk;
+    __syncthreads();
+  }
+  if (write_prefix && tid == 0) p.prefix[S] = static_cast<int32_t>(total);
+  if (a == b) return;
+
+  const uint32_t bar0 = smem_addr(smem + L.bar);
+  const int NS = p.stages, NQ = p.q_slots;
+  auto full_bar = [&](int i) { return bar0 + 8u * i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (NS + i); };
+  auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + i); };
+  auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + NQ + i); };
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta);
+  int* abort_flag = reinterpret_cast<int*>(misc + 34);
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), Hg);
+    }
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(qfull_bar(i), 1);
+      mbar_init(qempty_bar(i), Hg);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const int s_first = static_cast<int>(misc[32]);
+  const long long p_first = misc[33];
+  const uint32_t q_slot_bytes = (p.q_bytes + 127u) & ~127u;
+  const uint32_t qring = smem_addr(smem + L.qring);
+  const uint32_t stages = smem_addr(smem + L.stage);
+  const int G = p.group, H = p.num_heads, Hk = p.num_kv_heads, bs = p.block_size;
+
+  if (warp == Hg) {
+    // ---------------- producer ----------------
+    const T* kc = reinterpret_cast<const T*>(p.k_cache);
+    const T* vc = reinterpret_cast<const T*>(p.v_cache);
+    const T* qg = reinterpret_cast<const T*>(p.q);
+    int s = s_first;
+    long long ps = p_first;
+    int c = clamp_context(p, s, false);
+    long long ns = tiles_of(c);
+    int slot = segment_slot(a, b, ps, ps + ns);
+    int st = 0, qi = 0;
+    uint32_t ph = 0, qph = 0;
+    const int t = lane & 15;
+    const bool is_v = lane >= 16;
+    for (long long x = a; x < b; ++x) {
+      bool new_seq = (x == a);
+      while (x >= ps + ns) {
+        ps += ns;
+        ++s;
+        c = clamp_context(p, s, false);
+        ns = tiles_of(c);
+        new_seq = true;
+      }
+      if (new_seq) slot = segment_slot(a, b, ps, ps + ns);
+      const int j = static_cast<int>(x - ps);
+      const int tok0 = j * kTile;
+      const int nvalid = min(kTile, c - tok0);
+      const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
+                        ((slot + 1) << 2);
+      if (new_seq) {
+        if (!mbar_wait(qempty_bar(qi), qph ^ 1u)) {
+          report(p.error_flag, PA_DEVERR_TIMEOUT);
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t qb = qfull_bar(qi);
+          mbar_arrive_expect_tx(qb, p.q_bytes);
+          bulk_copy_g2s(qring + qi * q_slot_bytes, qg + ((size_t)s * H + (size_t)hg * Hg * G) * D,
+                        p.q_bytes, qb);
+        }
+        if (++qi == NQ) {
+          qi = 0;
+          qph ^= 1u;
+        }
+      }
+      // Block-table lookup for this lane's token (only valid tokens read the table).
+      bool ok = t < nvalid;
+      long long phys = 0;
+      if (ok) {
+        const int tok = tok0 + t;
+        phys = __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + tok / bs);
+        if (p.num_physical_blocks > 0 && (phys < 0 || phys >= p.num_physical_blocks)) {
+          report(p.error_flag, PA_DEVERR_BLOCK_ID);
+          ok = false;
+        }
+      }
+      const unsigned copies = __ballot_sync(0xffffffffu, ok);
+      if (!mbar_wait(empty_bar(st), ph ^ 1u)) {
+        report(p.error_flag, PA_DEVERR_TIMEOUT);
+        break;
+      }
+      if (lane == 0) {
+        meta[st] = StageMeta{s, tok0, nvalid, flags};
+        mbar_arrive_expect_tx(full_bar(st), __popc(copies) * p.row_bytes);
+      }
+      __syncwarp();
+      if (ok) {
+        const int tok = tok0 + t;
+        const size_t row = ((size_t)phys * bs + tok % bs) * Hk + (size_t)hg * Hg;
+        const T* src = (is_v ? vc : kc) + row * D;
+        const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
+        bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
+      }
+      if (++st == NS) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
+  } else {
+    // ---------------- consumers ----------------
+    const int w = warp;
+    const int kv_head = hg * Hg + w;
+    int st = 0, qi = 0;
+    uint32_t ph = 0, qph = 0;
+    constexpr bool kMma = (sizeof(T) == 2);
+    typename std::conditional<kMma, MmaConsumer<D>, SimtConsumer<D, GMAX>>::type cons;
+    for (long long x = a; x < b; ++x) {
+      if (!mbar_wait(full_bar(st), ph)) {
+        report(p.error_flag, PA_DEVERR_TIMEOUT);
+        break;
+      }
+      const StageMeta mt = meta[st];
+      if (mt.flags & kSegBegin) {
+        if (!mbar_wait(qfull_bar(qi), qph)) {
+          report(p.error_flag, PA_DEVERR_TIMEOUT);
+          break;
+        }
+        cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty_bar(qi));
+        if (++qi == NQ) {
+          qi = 0;
+          qph ^= 1u;
+        }
+      }
+      const uint32_t k_base = stages + st * p.stage_bytes + w * D * (uint32_t)sizeof(T);
+      const uint32_t v_base = k_base + kTile * p.pitch;
+      if constexpr (kMma) {
+        cons.tile(k_base, v_base, p.pitch, mt.nvalid, p.scale_log2, lane);
+      } else {
+        const unsigned char* kb = smem + L.stage + st * p.stage_bytes + w * D * sizeof(T);
+        cons.tile(kb, kb + kTile * p.pitch, p.pitch, mt.nvalid, p.scale_log2, G, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(st));
+      if (mt.flags & kSegEnd) cons.finish(p, mt.seq, kv_head, ((mt.flags >> 2) & 3) - 1, r, lane);
+      if (++st == NS) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  (void)abort_flag;
+  (void)Hk;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 2: log-sum-exp merge of cut sequences; zero rows for empty ones.
+// ---------------------------------------------------------------------------
+struct MergeParams {
+  void* out;
+  const int32_t* prefix;
+  const float* part_ml;
+  const float* part_o;
+  int num_seqs, num_heads, num_ranges;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) pa_merge_kernel(const MergeParams p) {
+  const int s = blockIdx.x;
+  const int H = p.num_heads;
+  const long long R = p.num_ranges;
+  const long long p0 = p.prefix[s], p1 = p.prefix[s + 1], total = p.prefix[p.num_seqs];
+  T* out = reinterpret_cast<T*>(p.out) + (size_t)s * H * D;
+  if (p1 == p0) {
+    for (int i = threadIdx.x; i < H * D; i += blockDim.x) out[i] = T(0.f);
+    return;
+  }
+  const long long r0 = range_of_tile(p0, total, R), r1 = range_of_tile(p1 - 1, total, R);
+  if (r0 == r1) return;
+  for (int i = threadIdx.x; i < H * D; i += blockDim.x) {
+    const int h = i / D, d = i % D;
+    float big_m = -INFINITY;
+    for (long long r = r0; r <= r1; ++r) {
+      if (range_start(r, total, R) == range_start(r + 1, total, R)) continue;
+      const int slot = partial_slot_of_range(r, p0, total, R);
+      big_m = fmaxf(big_m, p.part_ml[((r * 2 + slot) * H + h) * 2]);
+    }
+    float num = 0.f, den = 0.f;
+    for (long long r = r0; r <= r1; ++r) {
+      if (range_start(r, total, R) == range_start(r + 1, total, R)) continue;
+      const int slot = partial_slot_of_range(r, p0, total, R);
+      const size_t base = (size_t)(r * 2 + slot) * H + h;
+      const float wgt = exp2f(p.part_ml[base * 2] - big_m);
+      den += wgt * p.part_ml[base * 2 + 1];
+      num += wgt * p.part_o[base * D + d];
+    }
+    out[i] = T(num / den);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace {
+
+struct Plan {
+  int Hg, HG, R, stages, q_slots;
+  uint32_t row_bytes, pitch, q_bytes, stage_bytes, smem;
+  size_t ws_prefix, ws_ml, ws_o, ws_total;
+};
+
+size_t workspace_layout(int num_seqs, int num_heads, int head_size, int R, Plan* pl) {
+  const size_t prefix = align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 256);
+  const size_t ml = align_up(sizeof(float) * (size_t)R * 2 * num_heads * 2, 256);
+  const size_t o = align_up(sizeof(float) * (size_t)R * 2 * num_heads * head_size, 256);
+  if (pl) {
+    pl->ws_prefix = 0;
+    pl->ws_ml = prefix;
+    pl->ws_o = prefix + ml;
+    pl->ws_total = prefix + ml + o;
+  }
+  return prefix + ml + o;
+}
+
+int default_ranges(const DeviceInfo& dev, int HG) {
+  const int r = dev.sm_count / HG;
+  return r < 1 ? 1 : r;
+}
+
+int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int elt,
+              int num_ranges, const DeviceInfo& dev, Plan* pl) {
+  const int G = num_heads / num_kv_heads;
+  pl->Hg = num_kv_heads <= kMaxGroupHeads ? num_kv_heads : kMaxGroupHeads;
+  pl->HG = num_kv_heads / pl->Hg;
+  pl->R = num_ranges > 0 ? num_ranges : default_ranges(dev, pl->HG);
+  pl->row_bytes = (uint32_t)(pl->Hg * head_size * elt);
+  pl->pitch = pl->row_bytes + kRowSkew;
+  pl->q_bytes = (uint32_t)(pl->Hg * G * head_size * elt);
+  pl->stage_bytes = 2u * kTile * pl->pitch;
+  pl->stages = 0;
+  const int pref[][2] = {{6, 2}, {5, 2}, {4, 2}, {3, 2}, {3, 1}, {2, 2}, {2, 1}};
+  for (auto& c : pref) {
+    const Layout L = make_layout(c[0], c[1], pl->q_bytes, pl->stage_bytes);
+    if ((int)L.total <= dev.max_smem_optin) {
+      pl->stages = c[0];
+      pl->q_slots = c[1];
+      pl->smem = L.total;
+      break;
+    }
+  }
+  if (pl->stages == 0)
+    return fail(PA_ERR_UNSUPPORTED, "decode stages (%u bytes each) do not fit in %d bytes of shared memory",
+                pl->stage_bytes, dev.max_smem_optin);
+  workspace_layout(num_seqs, num_heads, head_size, pl->R, pl);
+  return PA_OK;
+}
+
+int validate(const void* out, const void* query, const void* k_cache, const void* v_cache,
+             const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads,
+             int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq, float scale,
+             int dtype, int num_physical_blocks, int num_ranges) {
+  if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: null tensor pointer");
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: sizes must be positive");
+  if (num_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: num_heads %d not a multiple of num_kv_heads %d",
+                num_heads, num_kv_heads);
+  if (num_heads / num_kv_heads > kMaxQueryGroup)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: query group %d > %d", num_heads / num_kv_heads,
+                kMaxQueryGroup);
+  if (num_kv_heads > kMaxGroupHeads && num_kv_heads % kMaxGroupHeads != 0)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: num_kv_heads %d > 8 must be a multiple of 8",
+                num_kv_heads);
+  if (head_size != 64 && head_size != 128)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: head_size %d (built: 64, 128)", head_size);
+  if (block_size > 4096) return fail(PA_ERR_UNSUPPORTED, "pa_decode: block_size %d > 4096", block_size);
+  if ((long long)max_blocks_per_seq * block_size > (1ll << 30))
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: max context %lld too large",
+                (long long)max_blocks_per_seq * block_size);
+  if (dtype != PA_F32 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype %d", dtype);
+  if (!aligned(out, 16) || !aligned(query, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: tensors must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "pa_decode: scale not finite");
+  if (num_physical_blocks < 0 || num_ranges < 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_decode: negative num_physical_blocks or num_ranges");
+  return PA_OK;
+}
+
+template <typename T, int D, int GMAX>
+int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream,
+                 MergeParams mp) {
+  static bool configured[64] = {false};
+  auto kern = pa_decode_kernel<T, D, GMAX>;
+  if (!configured[dev]) {
+    DeviceInfo info{};
+    int rc = current_device_info(&info);
+    if (rc != PA_OK) return rc;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem_optin);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode smem)");
+    configured[dev] = true;
+  }
+  const dim3 grid(pl.R * pl.HG), block(32 * (pl.Hg + 1));
+  kern<<<grid, block, pl.smem, stream>>>(prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch pa_decode_kernel");
+  pa_merge_kernel<T, D><<<dim3(mp.num_seqs), dim3(256), 0, stream>>>(mp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch pa_merge_kernel");
+  return PA_OK;
+}
+
+template <typename T, int D>
+int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream,
+                 MergeParams mp) {
+  if constexpr (sizeof(T) == 2) {
+    return launch_typed<T, D, 8>(prm, pl, dev, stream, mp);  // the MMA consumer pads G to 8
+  } else {
+    const int G = prm.group;
+    if (G <= 1) return launch_typed<T, D, 1>(prm, pl, dev, stream, mp);
+    if (G <= 2) return launch_typed<T, D, 2>(prm, pl, dev, stream, mp);
+    if (G <= 4) return launch_typed<T, D, 4>(prm, pl, dev, stream, mp);
+    return launch_typed<T, D, 8>(prm, pl, dev, stream, mp);
+  }
+}
+
+}  // namespace
+
+int decode_impl(void* out, const void* query, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                int num_heads, int num_kv_heads, int head_size, int block_size,
+                int max_blocks_per_seq, float scale, void* stream, int dtype,
+                int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                int32_t* error_flag) {
+  clear_error();
+  int rc = validate(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
+                    num_kv_heads, head_size, block_size, max_blocks_per_seq, scale, dtype,
+                    num_physical_blocks, num_ranges);
+  if (rc != PA_OK) return rc;
+  DeviceInfo dev{};
+  rc = current_device_info(&dev);
+  if (rc != PA_OK) return rc;
+  const int elt = dtype == PA_F32 ? 4 : 2;
+  Plan pl{};
+  rc = make_plan(num_seqs, num_heads, num_kv_heads, head_size, elt, num_ranges, dev, &pl);
+  if (rc != PA_OK) return rc;
+  if (workspace == nullptr) {
+    rc = library_workspace(pl.ws_total, &workspace);
+    if (rc != PA_OK) return rc;
+  } else {
+    if (workspace_bytes < pl.ws_total)
+      return fail(PA_ERR_WORKSPACE, "pa_decode: workspace of %zu bytes, %zu needed", workspace_bytes,
+                  pl.ws_total);
+    if (!aligned(workspace, 256)) return fail(PA_ERR_INVALID_ARG, "pa_decode: workspace not 256-byte aligned");
+  }
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  DecodeParams prm{};
+  prm.out = out;
+  prm.q = query;
+  prm.k_cache = k_cache;
+  prm.v_cache = v_cache;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.prefix = reinterpret_cast<int32_t*>(ws + pl.ws_prefix);
+  prm.part_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
+  prm.part_o = reinterpret_cast<float*>(ws + pl.ws_o);
+  prm.error_flag = error_flag;
+  prm.num_seqs = num_seqs;
+  prm.num_heads = num_heads;
+  prm.num_kv_heads = num_kv_heads;
+  prm.group = num_heads / num_kv_heads;
+  prm.block_size = block_size;
+  prm.max_blocks_per_seq = max_blocks_per_seq;
+  prm.heads_per_cta = pl.Hg;
+  prm.num_head_groups = pl.HG;
+  prm.num_ranges = pl.R;
+  prm.num_physical_blocks = num_physical_blocks;
+  prm.stages = pl.stages;
+  prm.q_slots = pl.q_slots;
+  prm.row_bytes = pl.row_bytes;
+  prm.pitch = pl.pitch;
+  prm.q_bytes = pl.q_bytes;
+  prm.stage_bytes = pl.stage_bytes;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  MergeParams mp{};
+  mp.out = out;
+  mp.prefix = prm.prefix;
+  mp.part_ml = prm.part_ml;
+  mp.part_o = prm.part_o;
+  mp.num_seqs = num_seqs;
+  mp.num_heads = num_heads;
+  mp.num_ranges = pl.R;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == PA_BF16) {
+    return head_size == 64 ? launch_dtype<__nv_bfloat16, 64>(prm, pl, dev.device, st, mp)
+                           : launch_dtype<__nv_bfloat16, 128>(prm, pl, dev.device, st, mp);
+  }
+  return head_size == 64 ? launch_dtype<float, 64>(prm, pl, dev.device, st, mp)
+                         : launch_dtype<float, 128>(prm, pl, dev.device, st, mp);
+}
+
+size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                             int num_ranges) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || num_ranges < 0 ||
+      num_heads % num_kv_heads != 0)
+    return 0;
+  int R = num_ranges;
+  if (R == 0) {
+    DeviceInfo dev{};
+    if (current_device_info(&dev) != PA_OK) return 0;
+    const int Hg = num_kv_heads <= kMaxGroupHeads ? num_kv_heads : kMaxGroupHeads;
+    R = default_ranges(dev, num_kv_heads / Hg);
+  }
+  return workspace_layout(num_seqs, num_heads, head_size, R, nullptr);
+}
+
+}  // namespace pa
+
+extern "C" int pa_decode(void* out, const void* query, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                         int num_heads, int num_kv_heads, int head_size, int block_size,
+                         int max_blocks_per_seq, float scale, void* stream, int dtype) {
+  return pa::decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                         num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                         stream, dtype, 0, nullptr, 0, 0, nullptr);
+}
+
+extern "C" int pa_decode_ws(void* out, const void* query, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                            int block_size, int max_blocks_per_seq, float scale, void* stream,
+                            int dtype, void* workspace, size_t workspace_bytes) {
+  if (workspace == nullptr) {
+    pa::clear_error();
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_ws: null workspace");
+  }
+  return pa::decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                         num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                         stream, dtype, 0, workspace, workspace_bytes, 0, nullptr);
+}
+
+extern "C" int pa_decode_ex(void* out, const void* query, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                            int block_size, int max_blocks_per_seq, float scale, void* stream,
+                            int dtype, int num_physical_blocks, void* workspace,
+                            size_t workspace_bytes, int num_ranges, int32_t* error_flag) {
+  return pa::decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                         num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                         stream, dtype, num_physical_blocks, workspace, workspace_bytes, num_ranges,
+                         error_flag);
+}
+
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                           int head_size, int num_ranges) {
+  return pa::decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, num_ranges);
+}

@@ -1,0 +1,98 @@
+// Cache write ("reshape_and_cache"): scatter one step's new K/V rows into the
+// paged pool through slot_mapping.
+//
+// Follows section 2 item 4 of "vLLM three-process architecture and the
+// PagedAttention kernel" (the new token joins its sequence's current physical
+// block) and section 4 item 3, which calls the kernel's access pattern a
+// gather-scatter: decode gathers through the block table, this kernel scatters
+// through the slot of each new token.
+//
+// In the [block, slot, kv_head, dim] pool one token's K (or V) for all KV heads
+// is a single contiguous row of num_kv_heads * head_size elements at row index
+// `slot` (block * block_size + offset).  So the scatter is a byte copy of whole
+// rows with 16-byte vector accesses; one CTA per token copies its K and V rows.
+#include <cuda_runtime.h>
+
+#include "../../include/pagedattn.h"
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+__global__ void __launch_bounds__(128) pa_write_cache_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+    const int64_t* __restrict__ slot_mapping, uint4* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, int num_tokens, int row_vecs, long long num_slots,
+    int32_t* error_flag) {
+  for (int i = blockIdx.x; i < num_tokens; i += gridDim.x) {
+    const long long slot = slot_mapping[i];
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (threadIdx.x == 0) report(error_flag, PA_DEVERR_SLOT);
+      continue;
+    }
+    const uint4* ks = k_new + (size_t)i * row_vecs;
+    const uint4* vs = v_new + (size_t)i * row_vecs;
+    uint4* kd = k_cache + (size_t)slot * row_vecs;
+    uint4* vd = v_cache + (size_t)slot * row_vecs;
+    for (int j = threadIdx.x; j < row_vecs; j += blockDim.x) {
+      const uint4 kv = __ldg(ks + j);
+      const uint4 vv = __ldg(vs + j);
+      kd[j] = kv;
+      vd[j] = vv;
+    }
+  }
+}
+
+int write_cache_impl(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                     void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
+                     int head_size, int block_size, int num_physical_blocks, void* stream,
+                     int dtype, int32_t* error_flag) {
+  clear_error();
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+    return fail(PA_ERR_INVALID_ARG, "pa_write_cache: null tensor pointer");
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+      num_physical_blocks <= 0)
+    return fail(PA_ERR_INVALID_ARG, "pa_write_cache: sizes must be positive");
+  if (dtype != PA_F32 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "pa_write_cache: dtype %d", dtype);
+  const long long row_bytes = (long long)num_kv_heads * head_size * (dtype == PA_F32 ? 4 : 2);
+  if (row_bytes % 16 != 0)
+    return fail(PA_ERR_UNSUPPORTED, "pa_write_cache: row of %lld bytes is not a multiple of 16",
+                row_bytes);
+  if (row_bytes / 16 > (1 << 24)) return fail(PA_ERR_UNSUPPORTED, "pa_write_cache: row too long");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return fail(PA_ERR_INVALID_ARG, "pa_write_cache: tensors must be 16-byte aligned");
+  if (num_tokens == 0) return PA_OK;
+  const long long num_slots = (long long)num_physical_blocks * block_size;
+  const int grid = num_tokens < 65535 ? num_tokens : 65535;
+  pa_write_cache_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens,
+      static_cast<int>(row_bytes / 16), num_slots, error_flag);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch pa_write_cache_kernel");
+  return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" int pa_write_cache(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                              void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
+                              int head_size, int block_size, int num_physical_blocks,
+                              void* stream, int dtype) {
+  return pa::write_cache_impl(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens,
+                              num_kv_heads, head_size, block_size, num_physical_blocks, stream,
+                              dtype, nullptr);
+}
+
+extern "C" int pa_write_cache_ex(const void* k_new, const void* v_new,
+                                 const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                 int num_tokens, int num_kv_heads, int head_size, int block_size,
+                                 int num_physical_blocks, void* stream, int dtype,
+                                 int32_t* error_flag) {
+  return pa::write_cache_impl(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens,
+                              num_kv_heads, head_size, block_size, num_physical_blocks, stream,
+                              dtype, error_flag);
+}
