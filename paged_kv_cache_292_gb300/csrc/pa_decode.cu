@@ -48,7 +48,8 @@ namespace pa {
 constexpr int kMaxGroupHeads = 8;  // KV heads per CTA (one consumer warp each)
 constexpr int kMaxQueryGroup = 8;  // query heads per KV head (MMA N extent)
 constexpr int kRowSkew = 16;       // bytes between staged rows beyond the row itself
-constexpr int kMaxStages = 6;
+constexpr int kMaxRowBytes = 2048;  // bytes of one staged token row (K or V)
+constexpr int kMaxRanges = 8192;    // bounds the merge kernel's range list in shared memory
 
 enum : int { kSegBegin = 1, kSegEnd = 2 };
 
@@ -427,6 +428,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes);
   long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
   const bool write_prefix = (r == 0 && hg == 0);
+  griddep_wait();  // inputs may come from the kernel just before (e.g. the cache write)
 
   // ---- Prologue: total tile count, this range, and its first sequence. ----
   long long total = 0;
@@ -465,6 +467,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     __syncthreads();
   }
   if (write_prefix && tid == 0) p.prefix[S] = static_cast<int32_t>(total);
+  griddep_launch_dependents();  // the merge kernel may get resident; it waits for our completion
   if (a == b) return;
 
   const uint32_t bar0 = smem_addr(smem + L.bar);
@@ -504,24 +507,47 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     long long ps = p_first;
     int c = clamp_context(p, s, false);
     long long ns = tiles_of(c);
-    int slot = segment_slot(a, b, ps, ps + ns);
+    // The next sequence's length is fetched one sequence ahead.
+    int c_next = (s + 1 < S) ? clamp_context(p, s + 1, false) : 0;
+    int slot = 0;
     int st = 0, qi = 0;
     uint32_t ph = 0, qph = 0;
     const int t = lane & 15;
     const bool is_v = lane >= 16;
+    // Block-table window of the current sequence: lane i holds entry cb+i in
+    // `cur` and cb+32+i in `nxt`.  The window slides one chunk at a time and the
+    // next chunk is loaded a chunk ahead, so lookups never wait on memory except
+    // at the first tile of a segment.
+    const int32_t* bt_row = nullptr;
+    int nblk = 0, cb = 0, cur = -1, nxt = -1;
+    auto table_entry = [&](int idx) -> int { return idx < nblk ? __ldg(bt_row + idx) : -1; };
     for (long long x = a; x < b; ++x) {
       bool new_seq = (x == a);
       while (x >= ps + ns) {
         ps += ns;
         ++s;
-        c = clamp_context(p, s, false);
+        c = c_next;
         ns = tiles_of(c);
+        c_next = (s + 1 < S) ? clamp_context(p, s + 1, false) : 0;
         new_seq = true;
       }
-      if (new_seq) slot = segment_slot(a, b, ps, ps + ns);
       const int j = static_cast<int>(x - ps);
       const int tok0 = j * kTile;
       const int nvalid = min(kTile, c - tok0);
+      const int blk0 = tok0 / bs;
+      if (new_seq) {
+        slot = segment_slot(a, b, ps, ps + ns);
+        bt_row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+        nblk = (c + bs - 1) / bs;
+        cb = blk0;
+        cur = table_entry(cb + lane);
+        nxt = table_entry(cb + 32 + lane);
+      }
+      while (blk0 >= cb + 32) {
+        cur = nxt;
+        cb += 32;
+        nxt = table_entry(cb + 32 + lane);
+      }
       const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
                         ((slot + 1) << 2);
       if (new_seq) {
@@ -540,16 +566,17 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
           qph ^= 1u;
         }
       }
-      // Block-table lookup for this lane's token (only valid tokens read the table).
+      // This lane's token -> physical block (a tile spans at most 16 blocks, so
+      // it always lies inside the 64-entry window).
+      const int tok = tok0 + t;
+      const int rel = tok / bs - cb;
+      const int e_cur = __shfl_sync(0xffffffffu, cur, rel & 31);
+      const int e_nxt = __shfl_sync(0xffffffffu, nxt, rel & 31);
+      long long phys = rel < 32 ? e_cur : e_nxt;
       bool ok = t < nvalid;
-      long long phys = 0;
-      if (ok) {
-        const int tok = tok0 + t;
-        phys = __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + tok / bs);
-        if (p.num_physical_blocks > 0 && (phys < 0 || phys >= p.num_physical_blocks)) {
-          report(p.error_flag, PA_DEVERR_BLOCK_ID);
-          ok = false;
-        }
+      if (ok && p.num_physical_blocks > 0 && (phys < 0 || phys >= p.num_physical_blocks)) {
+        report(p.error_flag, PA_DEVERR_BLOCK_ID);
+        ok = false;
       }
       const unsigned copies = __ballot_sync(0xffffffffu, ok);
       if (!mbar_wait(empty_bar(st), ph ^ 1u)) {
@@ -562,7 +589,6 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       }
       __syncwarp();
       if (ok) {
-        const int tok = tok0 + t;
         const size_t row = ((size_t)phys * bs + tok % bs) * Hk + (size_t)hg * Hg;
         const T* src = (is_v ? vc : kc) + row * D;
         const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
@@ -632,37 +658,64 @@ struct MergeParams {
   int num_seqs, num_heads, num_ranges;
 };
 
+constexpr int kMergeThreads = 256;
+constexpr int kMergeHeads = 32;  // query heads per merge CTA (grid.y covers the rest)
+
+// One CTA per (sequence, chunk of kMergeHeads query heads).  The list of
+// partials of a cut sequence (range r, slot) is computed once into shared
+// memory; each head's global maximum M and 1/L come next; each output element
+// is then sum_i 2^(m_i - M) O_i / L.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) pa_merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeParams p) {
+  extern __shared__ __align__(16) unsigned char msm[];
+  griddep_wait();  // partials and the prefix come from the decode kernel
   const int s = blockIdx.x;
   const int H = p.num_heads;
+  const int h0 = blockIdx.y * kMergeHeads;
+  const int hn = min(kMergeHeads, H - h0);
   const long long R = p.num_ranges;
   const long long p0 = p.prefix[s], p1 = p.prefix[s + 1], total = p.prefix[p.num_seqs];
-  T* out = reinterpret_cast<T*>(p.out) + (size_t)s * H * D;
+  T* out = reinterpret_cast<T*>(p.out) + ((size_t)s * H + h0) * D;
   if (p1 == p0) {
-    for (int i = threadIdx.x; i < H * D; i += blockDim.x) out[i] = T(0.f);
+    for (int i = threadIdx.x; i < hn * D; i += blockDim.x) out[i] = T(0.f);
     return;
   }
   const long long r0 = range_of_tile(p0, total, R), r1 = range_of_tile(p1 - 1, total, R);
-  if (r0 == r1) return;
-  for (int i = threadIdx.x; i < H * D; i += blockDim.x) {
-    const int h = i / D, d = i % D;
-    float big_m = -INFINITY;
-    for (long long r = r0; r <= r1; ++r) {
-      if (range_start(r, total, R) == range_start(r + 1, total, R)) continue;
-      const int slot = partial_slot_of_range(r, p0, total, R);
-      big_m = fmaxf(big_m, p.part_ml[((r * 2 + slot) * H + h) * 2]);
+  if (r0 == r1) return;  // finished inside one range by the decode kernel
+  const int np = static_cast<int>(r1 - r0 + 1);
+  float* big_m = reinterpret_cast<float*>(msm);
+  float* inv_l = big_m + kMergeHeads;
+  int* pidx = reinterpret_cast<int*>(inv_l + kMergeHeads);  // (r*2+slot), or -1 for an empty range
+  for (int i = threadIdx.x; i < np; i += blockDim.x) {
+    const long long r = r0 + i;
+    const bool empty = range_start(r, total, R) == range_start(r + 1, total, R);
+    pidx[i] = empty ? -1 : static_cast<int>(r * 2 + partial_slot_of_range(r, p0, total, R));
+  }
+  __syncthreads();
+  for (int hc = threadIdx.x; hc < hn; hc += blockDim.x) {
+    const int h = h0 + hc;
+    float m = -INFINITY;
+    for (int i = 0; i < np; ++i)
+      if (pidx[i] >= 0) m = fmaxf(m, p.part_ml[((size_t)pidx[i] * H + h) * 2]);
+    float l = 0.f;
+    for (int i = 0; i < np; ++i) {
+      if (pidx[i] < 0) continue;
+      const size_t b = ((size_t)pidx[i] * H + h) * 2;
+      l += exp2f(p.part_ml[b] - m) * p.part_ml[b + 1];
     }
-    float num = 0.f, den = 0.f;
-    for (long long r = r0; r <= r1; ++r) {
-      if (range_start(r, total, R) == range_start(r + 1, total, R)) continue;
-      const int slot = partial_slot_of_range(r, p0, total, R);
-      const size_t base = (size_t)(r * 2 + slot) * H + h;
-      const float wgt = exp2f(p.part_ml[base * 2] - big_m);
-      den += wgt * p.part_ml[base * 2 + 1];
-      num += wgt * p.part_o[base * D + d];
+    big_m[hc] = m;
+    inv_l[hc] = 1.f / l;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < hn * D; e += blockDim.x) {
+    const int hc = e / D, d = e % D, h = h0 + hc;
+    float acc = 0.f;
+    for (int i = 0; i < np; ++i) {
+      if (pidx[i] < 0) continue;
+      const size_t b = (size_t)pidx[i] * H + h;
+      acc += exp2f(p.part_ml[b * 2] - big_m[hc]) * p.part_o[b * D + d];
     }
-    out[i] = T(num / den);
+    out[e] = T(acc * inv_l[hc]);
   }
 }
 
@@ -690,6 +743,15 @@ size_t workspace_layout(int num_seqs, int num_heads, int head_size, int R, Plan*
   return prefix + ml + o;
 }
 
+// KV heads one CTA stages per token row: the largest divisor of num_kv_heads
+// that is at most 8 (one consumer warp each) and keeps the row within 2 KiB,
+// so three stages fit in shared memory.
+int heads_per_cta(int num_kv_heads, int head_size, int elt) {
+  for (int h = kMaxGroupHeads; h > 1; --h)
+    if (num_kv_heads % h == 0 && h * head_size * elt <= kMaxRowBytes) return h;
+  return 1;
+}
+
 int default_ranges(const DeviceInfo& dev, int HG) {
   const int r = dev.sm_count / HG;
   return r < 1 ? 1 : r;
@@ -698,7 +760,7 @@ int default_ranges(const DeviceInfo& dev, int HG) {
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int elt,
               int num_ranges, const DeviceInfo& dev, Plan* pl) {
   const int G = num_heads / num_kv_heads;
-  pl->Hg = num_kv_heads <= kMaxGroupHeads ? num_kv_heads : kMaxGroupHeads;
+  pl->Hg = heads_per_cta(num_kv_heads, head_size, elt);
   pl->HG = num_kv_heads / pl->Hg;
   pl->R = num_ranges > 0 ? num_ranges : default_ranges(dev, pl->HG);
   pl->row_bytes = (uint32_t)(pl->Hg * head_size * elt);
@@ -738,9 +800,6 @@ int validate(const void* out, const void* query, const void* k_cache, const void
   if (num_heads / num_kv_heads > kMaxQueryGroup)
     return fail(PA_ERR_UNSUPPORTED, "pa_decode: query group %d > %d", num_heads / num_kv_heads,
                 kMaxQueryGroup);
-  if (num_kv_heads > kMaxGroupHeads && num_kv_heads % kMaxGroupHeads != 0)
-    return fail(PA_ERR_UNSUPPORTED, "pa_decode: num_kv_heads %d > 8 must be a multiple of 8",
-                num_kv_heads);
   if (head_size != 64 && head_size != 128)
     return fail(PA_ERR_UNSUPPORTED, "pa_decode: head_size %d (built: 64, 128)", head_size);
   if (block_size > 4096) return fail(PA_ERR_UNSUPPORTED, "pa_decode: block_size %d > 4096", block_size);
@@ -752,9 +811,30 @@ int validate(const void* out, const void* query, const void* k_cache, const void
       !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return fail(PA_ERR_INVALID_ARG, "pa_decode: tensors must be 16-byte aligned");
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "pa_decode: scale not finite");
+  if (num_ranges > kMaxRanges)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: num_ranges %d > %d", num_ranges, kMaxRanges);
   if (num_physical_blocks < 0 || num_ranges < 0)
     return fail(PA_ERR_INVALID_ARG, "pa_decode: negative num_physical_blocks or num_ranges");
   return PA_OK;
+}
+
+// Launch with programmatic stream serialisation: the kernel may become
+// resident while its predecessor on the stream finishes; it calls
+// griddepcontrol.wait before touching anything that predecessor produces.
+template <typename Kernel, typename Params>
+cudaError_t launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       const Params& prm) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 template <typename T, int D, int GMAX>
@@ -771,12 +851,11 @@ int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode smem)");
     configured[dev] = true;
   }
-  const dim3 grid(pl.R * pl.HG), block(32 * (pl.Hg + 1));
-  kern<<<grid, block, pl.smem, stream>>>(prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg + 1)), pl.smem, stream, prm);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_decode_kernel");
-  pa_merge_kernel<T, D><<<dim3(mp.num_seqs), dim3(256), 0, stream>>>(mp);
-  e = cudaGetLastError();
+  const dim3 mgrid(mp.num_seqs, (mp.num_heads + kMergeHeads - 1) / kMergeHeads);
+  const size_t msmem = sizeof(float) * 2 * kMergeHeads + sizeof(int) * (size_t)mp.num_ranges;
+  e = launch_pdl(pa_merge_kernel<T, D>, mgrid, dim3(kMergeThreads), msmem, stream, mp);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_merge_kernel");
   return PA_OK;
 }
@@ -879,8 +958,9 @@ size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int 
   if (R == 0) {
     DeviceInfo dev{};
     if (current_device_info(&dev) != PA_OK) return 0;
-    const int Hg = num_kv_heads <= kMaxGroupHeads ? num_kv_heads : kMaxGroupHeads;
-    R = default_ranges(dev, num_kv_heads / Hg);
+    // The head grouping depends on the element size; size for bf16, whose
+    // larger groups leave more ranges per head group.
+    R = default_ranges(dev, num_kv_heads / heads_per_cta(num_kv_heads, head_size, 2));
   }
   return workspace_layout(num_seqs, num_heads, head_size, R, nullptr);
 }

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(128) pa_write_cache_kernel(
     const int64_t* __restrict__ slot_mapping, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, int num_tokens, int row_vecs, long long num_slots,
     int32_t* error_flag) {
+  griddep_wait();               // new rows may come from the kernel just before
+  griddep_launch_dependents();  // a following decode may get resident; it waits for us
   for (int i = blockIdx.x; i < num_tokens; i += gridDim.x) {
     const long long slot = slot_mapping[i];
     if (slot < 0) continue;  // padding token
@@ -49,7 +51,7 @@ int write_cache_impl(const void* k_new, const void* v_new, const int64_t* slot_m
                      int head_size, int block_size, int num_physical_blocks, void* stream,
                      int dtype, int32_t* error_flag) {
   clear_error();
-  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+  if (!k_cache || !v_cache || (num_tokens > 0 && (!k_new || !v_new || !slot_mapping)))
     return fail(PA_ERR_INVALID_ARG, "pa_write_cache: null tensor pointer");
   if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
       num_physical_blocks <= 0)
@@ -67,11 +69,19 @@ int write_cache_impl(const void* k_new, const void* v_new, const int64_t* slot_m
   if (num_tokens == 0) return PA_OK;
   const long long num_slots = (long long)num_physical_blocks * block_size;
   const int grid = num_tokens < 65535 ? num_tokens : 65535;
-  pa_write_cache_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens,
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, pa_write_cache_kernel, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      slot_mapping, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens,
       static_cast<int>(row_bytes / 16), num_slots, error_flag);
-  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_write_cache_kernel");
   return PA_OK;
 }

@@ -53,7 +53,7 @@ def _decode_args(**kw):
         (dict(block_size=0), binding.PA_ERR_INVALID_ARG),
         (dict(out=18), binding.PA_ERR_INVALID_ARG),  # misaligned
         (dict(scale=float("nan")), binding.PA_ERR_INVALID_ARG),
-        (dict(num_kv_heads=12, num_heads=12), binding.PA_ERR_UNSUPPORTED),
+        (dict(head_size=256), binding.PA_ERR_UNSUPPORTED),
     ],
 )
 def test_decode_rejects_bad_arguments_on_host(lib, kw, code):

@@ -97,7 +97,7 @@ def test_edge_context_lengths(block_size, dtype):
 @pytest.mark.parametrize(
     "heads, kv_heads, head_size",
     [(8, 8, 64), (8, 8, 128), (32, 8, 128), (64, 8, 128), (16, 2, 64), (8, 1, 128), (4, 4, 128),
-     (32, 16, 128), (48, 16, 64), (6, 2, 128), (7, 1, 64)],
+     (32, 16, 128), (48, 16, 64), (6, 2, 128), (7, 1, 64), (12, 12, 128), (24, 12, 64)],
 )
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_head_geometry(heads, kv_heads, head_size, dtype):
