@@ -35,6 +35,8 @@
 #include <float.h>
 #include <math.h>
 
+#include <stdlib.h>
+
 #include <cmath>
 #include <type_traits>
 
@@ -49,7 +51,8 @@ constexpr int kMaxGroupHeads = 8;  // KV heads per CTA (one consumer warp each)
 constexpr int kMaxQueryGroup = 8;  // query heads per KV head (MMA N extent)
 constexpr int kRowSkew = 16;       // bytes between staged rows beyond the row itself
 constexpr int kMaxRowBytes = 2048;  // bytes of one staged token row (K or V)
-constexpr int kMaxRanges = 8192;    // bounds the merge kernel's range list in shared memory
+constexpr int kDefaultPrefetchTiles = 4;
+constexpr int kMaxRanges = 4096;    // bounds the merge kernel's per-range lists (48 KiB of smem)
 
 enum : int { kSegBegin = 1, kSegEnd = 2 };
 
@@ -77,6 +80,7 @@ struct DecodeParams {
   int num_ranges;       // R
   int num_physical_blocks;
   int stages, q_slots;
+  int prefetch_tiles;  // L2 prefetch distance of the producer, in tiles (0 = off)
   uint32_t row_bytes, pitch, q_bytes, stage_bytes;
   float scale_log2;  // scale * log2(e)
 };
@@ -594,6 +598,24 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
         bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
       }
+      // L2 prefetch of the same rows `prefetch_tiles` tiles ahead in this
+      // sequence and range: the DRAM reads start while the shared-memory ring
+      // is still full, and the later bulk copy hits L2.
+      if (p.prefetch_tiles > 0) {
+        const int jp = j + p.prefetch_tiles;
+        if (jp < ns && x + p.prefetch_tiles < b) {
+          const int tokp = jp * kTile + t;
+          const int relp = tokp / bs - cb;
+          const int pc = __shfl_sync(0xffffffffu, cur, relp & 31);
+          const int pn = __shfl_sync(0xffffffffu, nxt, relp & 31);
+          const long long physp = relp < 32 ? pc : pn;
+          if (tokp < c && relp < 64 &&
+              (p.num_physical_blocks == 0 || (physp >= 0 && physp < p.num_physical_blocks))) {
+            const size_t row = ((size_t)physp * bs + tokp % bs) * Hk + (size_t)hg * Hg;
+            bulk_prefetch_l2((is_v ? vc : kc) + row * D, p.row_bytes);
+          }
+        }
+      }
       if (++st == NS) {
         st = 0;
         ph ^= 1u;
@@ -658,65 +680,66 @@ struct MergeParams {
   int num_seqs, num_heads, num_ranges;
 };
 
-constexpr int kMergeThreads = 256;
-constexpr int kMergeHeads = 32;  // query heads per merge CTA (grid.y covers the rest)
-
-// One CTA per (sequence, chunk of kMergeHeads query heads).  The list of
-// partials of a cut sequence (range r, slot) is computed once into shared
-// memory; each head's global maximum M and 1/L come next; each output element
-// is then sum_i 2^(m_i - M) O_i / L.
+// One CTA per (sequence, query head), one thread per output dimension.  For a
+// sequence cut across ranges, the partials' weights 2^(m_i - M) / L are formed
+// once in shared memory; each thread then sums its dimension of the partial
+// outputs with independent loads.  Sequences finished inside one range exit
+// at once; empty sequences get a zero row.
 template <typename T, int D>
-__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(D) pa_merge_kernel(const MergeParams p) {
   extern __shared__ __align__(16) unsigned char msm[];
   griddep_wait();  // partials and the prefix come from the decode kernel
-  const int s = blockIdx.x;
+  const int s = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const int H = p.num_heads;
-  const int h0 = blockIdx.y * kMergeHeads;
-  const int hn = min(kMergeHeads, H - h0);
   const long long R = p.num_ranges;
   const long long p0 = p.prefix[s], p1 = p.prefix[s + 1], total = p.prefix[p.num_seqs];
-  T* out = reinterpret_cast<T*>(p.out) + ((size_t)s * H + h0) * D;
+  T* out = reinterpret_cast<T*>(p.out) + ((size_t)s * H + h) * D;
   if (p1 == p0) {
-    for (int i = threadIdx.x; i < hn * D; i += blockDim.x) out[i] = T(0.f);
+    out[d] = T(0.f);
     return;
   }
   const long long r0 = range_of_tile(p0, total, R), r1 = range_of_tile(p1 - 1, total, R);
   if (r0 == r1) return;  // finished inside one range by the decode kernel
   const int np = static_cast<int>(r1 - r0 + 1);
-  float* big_m = reinterpret_cast<float*>(msm);
-  float* inv_l = big_m + kMergeHeads;
-  int* pidx = reinterpret_cast<int*>(inv_l + kMergeHeads);  // (r*2+slot), or -1 for an empty range
-  for (int i = threadIdx.x; i < np; i += blockDim.x) {
+  int* pidx = reinterpret_cast<int*>(msm);     // [np] partial index r*2+slot, -1 if range empty
+  float* wgt = reinterpret_cast<float*>(pidx + np);  // [np] m, then the final weight
+  float* lv = wgt + np;                              // [np] l
+  for (int i = d; i < np; i += blockDim.x) {
     const long long r = r0 + i;
     const bool empty = range_start(r, total, R) == range_start(r + 1, total, R);
-    pidx[i] = empty ? -1 : static_cast<int>(r * 2 + partial_slot_of_range(r, p0, total, R));
+    const int pi = empty ? -1 : static_cast<int>(r * 2 + partial_slot_of_range(r, p0, total, R));
+    pidx[i] = pi;
+    wgt[i] = pi < 0 ? -INFINITY : p.part_ml[((size_t)pi * H + h) * 2];
+    lv[i] = pi < 0 ? 0.f : p.part_ml[((size_t)pi * H + h) * 2 + 1];
   }
   __syncthreads();
-  for (int hc = threadIdx.x; hc < hn; hc += blockDim.x) {
-    const int h = h0 + hc;
+  if (d < 32) {
     float m = -INFINITY;
-    for (int i = 0; i < np; ++i)
-      if (pidx[i] >= 0) m = fmaxf(m, p.part_ml[((size_t)pidx[i] * H + h) * 2]);
+    for (int i = d; i < np; i += 32) m = fmaxf(m, wgt[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float l = 0.f;
-    for (int i = 0; i < np; ++i) {
-      if (pidx[i] < 0) continue;
-      const size_t b = ((size_t)pidx[i] * H + h) * 2;
-      l += exp2f(p.part_ml[b] - m) * p.part_ml[b + 1];
-    }
-    big_m[hc] = m;
-    inv_l[hc] = 1.f / l;
+    for (int i = d; i < np; i += 32) l += exp2f(wgt[i] - m) * lv[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    __syncwarp();
+    for (int i = d; i < np; i += 32) wgt[i] = pidx[i] < 0 ? 0.f : exp2f(wgt[i] - m) / l;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < hn * D; e += blockDim.x) {
-    const int hc = e / D, d = e % D, h = h0 + hc;
-    float acc = 0.f;
-    for (int i = 0; i < np; ++i) {
-      if (pidx[i] < 0) continue;
-      const size_t b = (size_t)pidx[i] * H + h;
-      acc += exp2f(p.part_ml[b * 2] - big_m[hc]) * p.part_o[b * D + d];
-    }
-    out[e] = T(acc * inv_l[hc]);
+  const float* po = p.part_o + (size_t)h * D + d;
+  const size_t pstride = (size_t)H * D;
+  float acc = 0.f;
+  int i = 0;
+  for (; i + 4 <= np; i += 4) {
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = pidx[i + k] < 0 ? 0.f : po[(size_t)pidx[i + k] * pstride];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc += wgt[i + k] * v[k];
   }
+  for (; i < np; ++i)
+    if (pidx[i] >= 0) acc += wgt[i] * po[(size_t)pidx[i] * pstride];
+  out[d] = T(acc);
 }
 
 // ---------------------------------------------------------------------------
@@ -750,6 +773,17 @@ int heads_per_cta(int num_kv_heads, int head_size, int elt) {
   for (int h = kMaxGroupHeads; h > 1; --h)
     if (num_kv_heads % h == 0 && h * head_size * elt <= kMaxRowBytes) return h;
   return 1;
+}
+
+// Producer L2 prefetch distance in tiles.  PA_L2_PREFETCH_TILES (0..32)
+// overrides the default; read once per process.
+int l2_prefetch_tiles() {
+  static const int v = [] {
+    const char* e = getenv("PA_L2_PREFETCH_TILES");
+    int x = e ? atoi(e) : kDefaultPrefetchTiles;
+    return x < 0 ? 0 : (x > 32 ? 32 : x);
+  }();
+  return v;
 }
 
 int default_ranges(const DeviceInfo& dev, int HG) {
@@ -853,9 +887,8 @@ int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
   }
   cudaError_t e = launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg + 1)), pl.smem, stream, prm);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_decode_kernel");
-  const dim3 mgrid(mp.num_seqs, (mp.num_heads + kMergeHeads - 1) / kMergeHeads);
-  const size_t msmem = sizeof(float) * 2 * kMergeHeads + sizeof(int) * (size_t)mp.num_ranges;
-  e = launch_pdl(pa_merge_kernel<T, D>, mgrid, dim3(kMergeThreads), msmem, stream, mp);
+  const size_t msmem = 12u * (size_t)mp.num_ranges;  // pidx, weight and l per partial
+  e = launch_pdl(pa_merge_kernel<T, D>, dim3(mp.num_seqs, mp.num_heads), dim3(D), msmem, stream, mp);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_merge_kernel");
   return PA_OK;
 }
@@ -926,6 +959,7 @@ int decode_impl(void* out, const void* query, const void* k_cache, const void* v
   prm.num_ranges = pl.R;
   prm.num_physical_blocks = num_physical_blocks;
   prm.stages = pl.stages;
+  prm.prefetch_tiles = l2_prefetch_tiles();
   prm.q_slots = pl.q_slots;
   prm.row_bytes = pl.row_bytes;
   prm.pitch = pl.pitch;
