@@ -35,8 +35,6 @@
 #include <float.h>
 #include <math.h>
 
-#include <stdlib.h>
-
 #include <cmath>
 #include <type_traits>
 
@@ -51,7 +49,6 @@ constexpr int kMaxGroupHeads = 8;  // KV heads per CTA (one consumer warp each)
 constexpr int kMaxQueryGroup = 8;  // query heads per KV head (MMA N extent)
 constexpr int kRowSkew = 16;       // bytes between staged rows beyond the row itself
 constexpr int kMaxRowBytes = 2048;  // bytes of one staged token row (K or V)
-constexpr int kDefaultPrefetchTiles = 4;
 constexpr int kMaxRanges = 4096;    // bounds the merge kernel's per-range lists (48 KiB of smem)
 
 enum : int { kSegBegin = 1, kSegEnd = 2 };
@@ -80,7 +77,6 @@ struct DecodeParams {
   int num_ranges;       // R
   int num_physical_blocks;
   int stages, q_slots;
-  int prefetch_tiles;  // L2 prefetch distance of the producer, in tiles (0 = off)
   uint32_t row_bytes, pitch, q_bytes, stage_bytes;
   float scale_log2;  // scale * log2(e)
 };
@@ -598,24 +594,6 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
         bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
       }
-      // L2 prefetch of the same rows `prefetch_tiles` tiles ahead in this
-      // sequence and range: the DRAM reads start while the shared-memory ring
-      // is still full, and the later bulk copy hits L2.
-      if (p.prefetch_tiles > 0) {
-        const int jp = j + p.prefetch_tiles;
-        if (jp < ns && x + p.prefetch_tiles < b) {
-          const int tokp = jp * kTile + t;
-          const int relp = tokp / bs - cb;
-          const int pc = __shfl_sync(0xffffffffu, cur, relp & 31);
-          const int pn = __shfl_sync(0xffffffffu, nxt, relp & 31);
-          const long long physp = relp < 32 ? pc : pn;
-          if (tokp < c && relp < 64 &&
-              (p.num_physical_blocks == 0 || (physp >= 0 && physp < p.num_physical_blocks))) {
-            const size_t row = ((size_t)physp * bs + tokp % bs) * Hk + (size_t)hg * Hg;
-            bulk_prefetch_l2((is_v ? vc : kc) + row * D, p.row_bytes);
-          }
-        }
-      }
       if (++st == NS) {
         st = 0;
         ph ^= 1u;
@@ -773,17 +751,6 @@ int heads_per_cta(int num_kv_heads, int head_size, int elt) {
   for (int h = kMaxGroupHeads; h > 1; --h)
     if (num_kv_heads % h == 0 && h * head_size * elt <= kMaxRowBytes) return h;
   return 1;
-}
-
-// Producer L2 prefetch distance in tiles.  PA_L2_PREFETCH_TILES (0..32)
-// overrides the default; read once per process.
-int l2_prefetch_tiles() {
-  static const int v = [] {
-    const char* e = getenv("PA_L2_PREFETCH_TILES");
-    int x = e ? atoi(e) : kDefaultPrefetchTiles;
-    return x < 0 ? 0 : (x > 32 ? 32 : x);
-  }();
-  return v;
 }
 
 int default_ranges(const DeviceInfo& dev, int HG) {
@@ -959,7 +926,6 @@ int decode_impl(void* out, const void* query, const void* k_cache, const void* v
   prm.num_ranges = pl.R;
   prm.num_physical_blocks = num_physical_blocks;
   prm.stages = pl.stages;
-  prm.prefetch_tiles = l2_prefetch_tiles();
   prm.q_slots = pl.q_slots;
   prm.row_bytes = pl.row_bytes;
   prm.pitch = pl.pitch;
