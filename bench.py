@@ -285,7 +285,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     ws_bytes = lib.pa_decode_workspace_size(S, H, Hk, D, 0)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # merge tickets start at zero
     P = binding._ptr
 
     def write(gg):

@@ -77,11 +77,13 @@ extern "C" {
  * Requirements: num_heads % num_kv_heads == 0 and num_heads / num_kv_heads <= 8;
  * head_size 64 or 128; block_size in [1, 4096]; query, out and both pools
  * 16-byte aligned.
- * Long sequences are split across CTAs and their partial softmax statistics
- * merged by a second log-sum-exp kernel; the scratch for that comes from a
- * per-device buffer the library allocates on first use and grows when a
- * larger batch needs it (cudaMalloc, which synchronises the device; use
- * pa_decode_ws to supply the scratch and never allocate).
+ * The batch's tiles of 16 tokens are split into equal ranges, one CTA each.
+ * A sequence cut by range boundaries leaves partial softmax statistics per
+ * range; the last CTA to finish one of its KV heads merges them by
+ * log-sum-exp in a second pass over the partials.  The scratch for that comes
+ * from a per-device buffer the library allocates (zero-filled) on first use
+ * and grows when a larger batch needs it (cudaMalloc, which synchronises the
+ * device; use pa_decode_ws to supply the scratch and never allocate).
  */
 int pa_decode(void* out, const void* query, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
@@ -99,8 +101,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
 /*
  * pa_decode_ws - pa_decode with caller-owned scratch (device memory of at
  * least pa_decode_workspace_size(...) bytes, 256-byte aligned).  Never
- * allocates.  The scratch may be reused by the next call on the same stream;
- * two calls that overlap in time must not share it.
+ * allocates.  The scratch must be zero-filled before its first use; every
+ * call that completes leaves it zero-filled again, so it can be reused by the
+ * next call on the same stream.  Two calls that overlap in time must not
+ * share it.  After a call that reported PA_DEVERR_TIMEOUT, zero it again.
  */
 int pa_decode_ws(void* out, const void* query, const void* k_cache, const void* v_cache,
                  const int32_t* block_tables, const int32_t* context_lens, int num_seqs,

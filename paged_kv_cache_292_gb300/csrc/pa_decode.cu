@@ -26,10 +26,13 @@
 //     registers (running max and sum in the exp2 domain), then
 //     O^T[D x 8] += V^T[D x 16] * P^T[16 x 8], with P^T obtained from the score
 //     fragment by movmatrix.  fp32: the same on CUDA cores.
-//   * A sequence wholly inside the range is written to `out` directly; a
-//     sequence cut by the range boundary leaves (m, l, O) partials.
-// Kernel 2 (pa_merge_kernel), one CTA per sequence: merges the partials of cut
-// sequences by log-sum-exp and zero-fills empty sequences.
+//   * A sequence wholly inside the range is written to `out` directly.  A
+//     sequence cut by range boundaries leaves one (m, l, O) partial per range
+//     and KV head; the warp that writes the last of them (an atomic ticket per
+//     sequence and KV head, no waiting) then merges them all by log-sum-exp:
+//     out = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i.  The ticket counters
+//     are reset by that warp, so the scratch is left zeroed for the next call.
+//   * Empty sequences get a zero row from the prologue.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <float.h>
@@ -49,7 +52,7 @@ constexpr int kMaxGroupHeads = 8;  // KV heads per CTA (one consumer warp each)
 constexpr int kMaxQueryGroup = 8;  // query heads per KV head (MMA N extent)
 constexpr int kRowSkew = 16;       // bytes between staged rows beyond the row itself
 constexpr int kMaxRowBytes = 2048;  // bytes of one staged token row (K or V)
-constexpr int kMaxRanges = 4096;    // bounds the merge kernel's per-range lists (48 KiB of smem)
+constexpr int kMaxRanges = 4096;    // bounds the partial-result scratch
 
 enum : int { kSegBegin = 1, kSegEnd = 2 };
 
@@ -57,7 +60,9 @@ struct StageMeta {
   int seq;     // sequence index
   int tok0;    // first token of the tile within the sequence
   int nvalid;  // valid tokens in the tile (1..16)
-  int flags;   // kSegBegin | kSegEnd | (output slot + 1) << 2
+  int flags;   // kSegBegin | kSegEnd | (output slot + 1) << 2 | (slot of range r0) << 4
+  int r0, r1;  // first and last range touching the sequence (cut sequences only)
+  int pad0, pad1;
 };
 
 struct DecodeParams {
@@ -67,7 +72,7 @@ struct DecodeParams {
   const void* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
-  int32_t* prefix;  // [num_seqs + 1] tile offsets (written by range 0's CTAs)
+  int32_t* counters;  // [num_seqs][num_kv_heads] merge tickets; zero between calls
   float* part_ml;   // [R][2][H][2]: (m in log2 units, l)
   float* part_o;    // [R][2][H][D]: un-normalised weighted V sums
   int32_t* error_flag;
@@ -93,7 +98,7 @@ PA_HD Layout make_layout(int stages, int q_slots, uint32_t q_bytes, uint32_t sta
   o += 8u * (2u * stages + 2u * q_slots);
   o = (o + 15u) & ~15u;
   L.meta = o;
-  o += 16u * stages;
+  o += 32u * stages;
   L.misc = o;
   o += 4u * 80u;
   o = (o + 127u) & ~127u;
@@ -413,6 +418,88 @@ struct SimtConsumer {
   }
 };
 
+// Zero output row of an empty sequence (16-byte stores; rows are 16-byte multiples).
+template <typename T, int D>
+__device__ void zero_row(const DecodeParams& p, int s) {
+  const size_t n16 = (size_t)p.num_heads * D * sizeof(T) / 16;
+  uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) + (size_t)s * p.num_heads * D);
+  for (size_t i = 0; i < n16; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Called by a consumer warp right after it wrote its partial (m, l, O) for
+// (seq, kv_head).  Takes a ticket; the warp holding the last of the r1-r0+1
+// tickets merges every partial of that sequence and KV head by log-sum-exp,
+// writes the output rows, and resets the ticket counter.  Nobody waits.
+template <typename T, int D>
+__device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, int r0, int r1,
+                                 int slot0, int lane) {
+  __threadfence();  // this warp's partial is visible before its ticket is
+  __syncwarp();
+  int* cnt = p.counters + (size_t)seq * p.num_kv_heads + kv_head;
+  int ticket = 0;
+  if (lane == 0) ticket = atomicAdd(cnt, 1);
+  ticket = __shfl_sync(0xffffffffu, ticket, 0);
+  if (ticket != r1 - r0) return;
+  __threadfence();  // every other partial is visible now
+  constexpr int DL = D / 32;  // output dims per lane
+  const int G = p.group, H = p.num_heads;
+  T* out = reinterpret_cast<T*>(p.out) + (size_t)seq * H * D;
+  for (int g = 0; g < G; ++g) {
+    const int h = kv_head * G + g;
+    float big_m = -INFINITY;
+    for (int rr = r0 + lane; rr <= r1; rr += 32) {
+      const int sl = rr == r0 ? slot0 : 0;
+      big_m = fmaxf(big_m, __ldcg(p.part_ml + (((size_t)rr * 2 + sl) * H + h) * 2));
+    }
+    big_m = warp_max_f(big_m);
+    float den = 0.f;
+    for (int rr = r0 + lane; rr <= r1; rr += 32) {
+      const int sl = rr == r0 ? slot0 : 0;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + ((size_t)rr * 2 + sl) * H + h);
+      den += exp2f(ml.x - big_m) * ml.y;
+    }
+    den = warp_sum_f(den);
+    float acc[DL];
+#pragma unroll
+    for (int i = 0; i < DL; ++i) acc[i] = 0.f;
+#pragma unroll 4
+    for (int rr = r0; rr <= r1; ++rr) {
+      const int sl = rr == r0 ? slot0 : 0;
+      const size_t base = ((size_t)rr * 2 + sl) * H + h;
+      const float wgt = exp2f(__ldcg(p.part_ml + base * 2) - big_m);
+      const float* po = p.part_o + base * D + lane * DL;
+      if constexpr (DL == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+        acc[0] += wgt * v.x;
+        acc[1] += wgt * v.y;
+        acc[2] += wgt * v.z;
+        acc[3] += wgt * v.w;
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+        acc[0] += wgt * v.x;
+        acc[1] += wgt * v.y;
+      }
+    }
+    const float inv = 1.f / den;
+#pragma unroll
+    for (int i = 0; i < DL; ++i) out[(size_t)h * D + lane * DL + i] = T(acc[i] * inv);
+  }
+  __syncwarp();
+  if (lane == 0) *cnt = 0;  // leave the counter zeroed for the next call
+}
+
 // ---------------------------------------------------------------------------
 // Kernel 1
 // ---------------------------------------------------------------------------
@@ -427,7 +514,6 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const int Hg = p.heads_per_cta;
   const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes);
   long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
-  const bool write_prefix = (r == 0 && hg == 0);
   griddep_wait();  // inputs may come from the kernel just before (e.g. the cache write)
 
   // ---- Prologue: total tile count, this range, and its first sequence. ----
@@ -435,14 +521,18 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   for (int base = 0; base < S; base += nthreads) {
     const int s = base + tid;
     long long n = (s < S) ? tiles_of(clamp_context(p, s, true)) : 0;
+    if (s < S && n == 0 && s % gridDim.x == blockIdx.x) zero_row<T, D>(p, s);
     n = warp_sum_ll(n);
     if (lane == 0) misc[warp] = n;
     __syncthreads();
     for (int w = 0; w < nwarps; ++w) total += misc[w];
     __syncthreads();
   }
-  const long long a = range_start(r, total, R), b = range_start(r + 1, total, R);
-  if (a == b && !write_prefix) return;
+  // Never more ranges than tiles, so no range is empty and a cut sequence
+  // has exactly r1 - r0 + 1 partials.
+  const long long Reff = total < R ? total : R;
+  if (r >= Reff) return;
+  const long long a = range_start(r, total, Reff), b = range_start(r + 1, total, Reff);
 
   long long run = 0;
   for (int base = 0; base < S; base += nthreads) {
@@ -456,19 +546,14 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     long long chunk = 0;
     for (int w = 0; w < nwarps; ++w) chunk += misc[w];
     const long long excl = before + incl - n;
-    if (s < S) {
-      if (write_prefix) p.prefix[s] = static_cast<int32_t>(excl);
-      if (n > 0 && excl <= a && a < excl + n) {
-        misc[32] = s;
-        misc[33] = excl;
-      }
+    if (s < S && n > 0 && excl <= a && a < excl + n) {
+      misc[32] = s;
+      misc[33] = excl;
     }
     run += chunk;
     __syncthreads();
   }
-  if (write_prefix && tid == 0) p.prefix[S] = static_cast<int32_t>(total);
-  griddep_launch_dependents();  // the merge kernel may get resident; it waits for our completion
-  if (a == b) return;
+  griddep_launch_dependents();  // the next kernel may get resident; it waits for our completion
 
   const uint32_t bar0 = smem_addr(smem + L.bar);
   const int NS = p.stages, NQ = p.q_slots;
@@ -509,7 +594,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     long long ns = tiles_of(c);
     // The next sequence's length is fetched one sequence ahead.
     int c_next = (s + 1 < S) ? clamp_context(p, s + 1, false) : 0;
-    int slot = 0;
+    int slot = 0, seg_r0 = 0, seg_r1 = 0, seg_slot0 = 0;
     int st = 0, qi = 0;
     uint32_t ph = 0, qph = 0;
     const int t = lane & 15;
@@ -537,6 +622,11 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const int blk0 = tok0 / bs;
       if (new_seq) {
         slot = segment_slot(a, b, ps, ps + ns);
+        if (slot >= 0) {
+          seg_r0 = static_cast<int>(range_of_tile(ps, total, Reff));
+          seg_r1 = static_cast<int>(range_of_tile(ps + ns - 1, total, Reff));
+          seg_slot0 = partial_slot_of_range(seg_r0, ps, total, Reff);
+        }
         bt_row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
         nblk = (c + bs - 1) / bs;
         cb = blk0;
@@ -549,7 +639,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         nxt = table_entry(cb + 32 + lane);
       }
       const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
-                        ((slot + 1) << 2);
+                        ((slot + 1) << 2) | (seg_slot0 << 4);
       if (new_seq) {
         if (!mbar_wait(qempty_bar(qi), qph ^ 1u)) {
           report(p.error_flag, PA_DEVERR_TIMEOUT);
@@ -584,7 +674,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         break;
       }
       if (lane == 0) {
-        meta[st] = StageMeta{s, tok0, nvalid, flags};
+        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, 0, 0};
         mbar_arrive_expect_tx(full_bar(st), __popc(copies) * p.row_bytes);
       }
       __syncwarp();
@@ -636,7 +726,11 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(st));
-      if (mt.flags & kSegEnd) cons.finish(p, mt.seq, kv_head, ((mt.flags >> 2) & 3) - 1, r, lane);
+      if (mt.flags & kSegEnd) {
+        const int slot = ((mt.flags >> 2) & 3) - 1;
+        cons.finish(p, mt.seq, kv_head, slot, r, lane);
+        if (slot >= 0) arrive_and_merge<T, D>(p, mt.seq, kv_head, mt.r0, mt.r1, (mt.flags >> 4) & 1, lane);
+      }
       if (++st == NS) {
         st = 0;
         ph ^= 1u;
@@ -645,79 +739,6 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   }
   (void)abort_flag;
   (void)Hk;
-}
-
-// ---------------------------------------------------------------------------
-// Kernel 2: log-sum-exp merge of cut sequences; zero rows for empty ones.
-// ---------------------------------------------------------------------------
-struct MergeParams {
-  void* out;
-  const int32_t* prefix;
-  const float* part_ml;
-  const float* part_o;
-  int num_seqs, num_heads, num_ranges;
-};
-
-// One CTA per (sequence, query head), one thread per output dimension.  For a
-// sequence cut across ranges, the partials' weights 2^(m_i - M) / L are formed
-// once in shared memory; each thread then sums its dimension of the partial
-// outputs with independent loads.  Sequences finished inside one range exit
-// at once; empty sequences get a zero row.
-template <typename T, int D>
-__global__ void __launch_bounds__(D) pa_merge_kernel(const MergeParams p) {
-  extern __shared__ __align__(16) unsigned char msm[];
-  griddep_wait();  // partials and the prefix come from the decode kernel
-  const int s = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-  const int H = p.num_heads;
-  const long long R = p.num_ranges;
-  const long long p0 = p.prefix[s], p1 = p.prefix[s + 1], total = p.prefix[p.num_seqs];
-  T* out = reinterpret_cast<T*>(p.out) + ((size_t)s * H + h) * D;
-  if (p1 == p0) {
-    out[d] = T(0.f);
-    return;
-  }
-  const long long r0 = range_of_tile(p0, total, R), r1 = range_of_tile(p1 - 1, total, R);
-  if (r0 == r1) return;  // finished inside one range by the decode kernel
-  const int np = static_cast<int>(r1 - r0 + 1);
-  int* pidx = reinterpret_cast<int*>(msm);     // [np] partial index r*2+slot, -1 if range empty
-  float* wgt = reinterpret_cast<float*>(pidx + np);  // [np] m, then the final weight
-  float* lv = wgt + np;                              // [np] l
-  for (int i = d; i < np; i += blockDim.x) {
-    const long long r = r0 + i;
-    const bool empty = range_start(r, total, R) == range_start(r + 1, total, R);
-    const int pi = empty ? -1 : static_cast<int>(r * 2 + partial_slot_of_range(r, p0, total, R));
-    pidx[i] = pi;
-    wgt[i] = pi < 0 ? -INFINITY : p.part_ml[((size_t)pi * H + h) * 2];
-    lv[i] = pi < 0 ? 0.f : p.part_ml[((size_t)pi * H + h) * 2 + 1];
-  }
-  __syncthreads();
-  if (d < 32) {
-    float m = -INFINITY;
-    for (int i = d; i < np; i += 32) m = fmaxf(m, wgt[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float l = 0.f;
-    for (int i = d; i < np; i += 32) l += exp2f(wgt[i] - m) * lv[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    __syncwarp();
-    for (int i = d; i < np; i += 32) wgt[i] = pidx[i] < 0 ? 0.f : exp2f(wgt[i] - m) / l;
-  }
-  __syncthreads();
-  const float* po = p.part_o + (size_t)h * D + d;
-  const size_t pstride = (size_t)H * D;
-  float acc = 0.f;
-  int i = 0;
-  for (; i + 4 <= np; i += 4) {
-    float v[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = pidx[i + k] < 0 ? 0.f : po[(size_t)pidx[i + k] * pstride];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc += wgt[i + k] * v[k];
-  }
-  for (; i < np; ++i)
-    if (pidx[i] >= 0) acc += wgt[i] * po[(size_t)pidx[i] * pstride];
-  out[d] = T(acc);
 }
 
 // ---------------------------------------------------------------------------
@@ -731,8 +752,9 @@ struct Plan {
   size_t ws_prefix, ws_ml, ws_o, ws_total;
 };
 
-size_t workspace_layout(int num_seqs, int num_heads, int head_size, int R, Plan* pl) {
-  const size_t prefix = align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 256);
+size_t workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_size, int R,
+                        Plan* pl) {
+  const size_t prefix = align_up(sizeof(int32_t) * (size_t)num_seqs * num_kv_heads, 256);
   const size_t ml = align_up(sizeof(float) * (size_t)R * 2 * num_heads * 2, 256);
   const size_t o = align_up(sizeof(float) * (size_t)R * 2 * num_heads * head_size, 256);
   if (pl) {
@@ -782,7 +804,7 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int 
   if (pl->stages == 0)
     return fail(PA_ERR_UNSUPPORTED, "decode stages (%u bytes each) do not fit in %d bytes of shared memory",
                 pl->stage_bytes, dev.max_smem_optin);
-  workspace_layout(num_seqs, num_heads, head_size, pl->R, pl);
+  workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, pl->R, pl);
   return PA_OK;
 }
 
@@ -839,8 +861,7 @@ cudaError_t launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStre
 }
 
 template <typename T, int D, int GMAX>
-int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream,
-                 MergeParams mp) {
+int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream) {
   static bool configured[64] = {false};
   auto kern = pa_decode_kernel<T, D, GMAX>;
   if (!configured[dev]) {
@@ -854,23 +875,19 @@ int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
   }
   cudaError_t e = launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg + 1)), pl.smem, stream, prm);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_decode_kernel");
-  const size_t msmem = 12u * (size_t)mp.num_ranges;  // pidx, weight and l per partial
-  e = launch_pdl(pa_merge_kernel<T, D>, dim3(mp.num_seqs, mp.num_heads), dim3(D), msmem, stream, mp);
-  if (e != cudaSuccess) return cuda_fail(e, "launch pa_merge_kernel");
   return PA_OK;
 }
 
 template <typename T, int D>
-int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream,
-                 MergeParams mp) {
+int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream) {
   if constexpr (sizeof(T) == 2) {
-    return launch_typed<T, D, 8>(prm, pl, dev, stream, mp);  // the MMA consumer pads G to 8
+    return launch_typed<T, D, 8>(prm, pl, dev, stream);  // the MMA consumer pads G to 8
   } else {
     const int G = prm.group;
-    if (G <= 1) return launch_typed<T, D, 1>(prm, pl, dev, stream, mp);
-    if (G <= 2) return launch_typed<T, D, 2>(prm, pl, dev, stream, mp);
-    if (G <= 4) return launch_typed<T, D, 4>(prm, pl, dev, stream, mp);
-    return launch_typed<T, D, 8>(prm, pl, dev, stream, mp);
+    if (G <= 1) return launch_typed<T, D, 1>(prm, pl, dev, stream);
+    if (G <= 2) return launch_typed<T, D, 2>(prm, pl, dev, stream);
+    if (G <= 4) return launch_typed<T, D, 4>(prm, pl, dev, stream);
+    return launch_typed<T, D, 8>(prm, pl, dev, stream);
   }
 }
 
@@ -911,7 +928,7 @@ int decode_impl(void* out, const void* query, const void* k_cache, const void* v
   prm.v_cache = v_cache;
   prm.block_tables = block_tables;
   prm.context_lens = context_lens;
-  prm.prefix = reinterpret_cast<int32_t*>(ws + pl.ws_prefix);
+  prm.counters = reinterpret_cast<int32_t*>(ws + pl.ws_prefix);
   prm.part_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
   prm.part_o = reinterpret_cast<float*>(ws + pl.ws_o);
   prm.error_flag = error_flag;
@@ -932,21 +949,13 @@ int decode_impl(void* out, const void* query, const void* k_cache, const void* v
   prm.q_bytes = pl.q_bytes;
   prm.stage_bytes = pl.stage_bytes;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  MergeParams mp{};
-  mp.out = out;
-  mp.prefix = prm.prefix;
-  mp.part_ml = prm.part_ml;
-  mp.part_o = prm.part_o;
-  mp.num_seqs = num_seqs;
-  mp.num_heads = num_heads;
-  mp.num_ranges = pl.R;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == PA_BF16) {
-    return head_size == 64 ? launch_dtype<__nv_bfloat16, 64>(prm, pl, dev.device, st, mp)
-                           : launch_dtype<__nv_bfloat16, 128>(prm, pl, dev.device, st, mp);
+    return head_size == 64 ? launch_dtype<__nv_bfloat16, 64>(prm, pl, dev.device, st)
+                           : launch_dtype<__nv_bfloat16, 128>(prm, pl, dev.device, st);
   }
-  return head_size == 64 ? launch_dtype<float, 64>(prm, pl, dev.device, st, mp)
-                         : launch_dtype<float, 128>(prm, pl, dev.device, st, mp);
+  return head_size == 64 ? launch_dtype<float, 64>(prm, pl, dev.device, st)
+                         : launch_dtype<float, 128>(prm, pl, dev.device, st);
 }
 
 size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
@@ -962,7 +971,7 @@ size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int 
     // larger groups leave more ranges per head group.
     R = default_ranges(dev, num_kv_heads / heads_per_cta(num_kv_heads, head_size, 2));
   }
-  return workspace_layout(num_seqs, num_heads, head_size, R, nullptr);
+  return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, R, nullptr);
 }
 
 }  // namespace pa

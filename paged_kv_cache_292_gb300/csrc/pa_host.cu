@@ -80,6 +80,11 @@ int library_workspace(size_t bytes, void** ptr) {
       g_ws_ptr[dev] = nullptr;
       return cuda_fail(e, "cudaMalloc(workspace)");
     }
+    // Decode's merge tickets must start at zero; every completed call leaves
+    // them zero again.
+    e = cudaMemset(g_ws_ptr[dev], 0, want);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
     g_ws_bytes[dev] = want;
   }
   *ptr = g_ws_ptr[dev];

@@ -153,11 +153,17 @@ def test_decode_ws_matches_and_checks_size():
     S, H, D = w.q.shape
     Hk = w.spec.num_kv_heads
     need = binding.pa_decode_workspace_size(S, H, Hk, D)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(g["q"])
     binding.pa_decode_ws(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"], g["context_lens"], S, H, Hk,
                          D, w.spec.block_size, w.max_blocks_per_seq, w.scale, None, None, ws, need)
     ref = binding.decode(g["q"], g["k_cache"], g["v_cache"], g["block_tables"], g["context_lens"], w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    # Every call leaves the merge tickets zeroed, so the scratch is reusable as is.
+    assert int(ws[:4 * S * Hk].view(torch.int32).abs().sum()) == 0
+    binding.pa_decode_ws(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"], g["context_lens"], S, H, Hk,
+                         D, w.spec.block_size, w.max_blocks_per_seq, w.scale, None, None, ws, need)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
     with pytest.raises(binding.PagedAttnError) as e:
