@@ -408,7 +408,7 @@ def run_ours(args):
             "replicas": world,
         },
         "roofline": {
-            "kernel": "pa_decode (decode kernel + LSE merge kernel, one C-ABI call)",
+            "kernel": "pa_decode_kernel (one launch per pa_decode call; split sequences merged in-kernel)",
             "bound": "hbm",
             "achieved": achieved,
             "peak": peak,
@@ -422,7 +422,7 @@ def run_ours(args):
                 "ms_per_step": e2e_ms,
                 "note": "per-step inputs (q, new K/V, slots, tables, lengths) from pinned host, output back; "
                         "the paged pool is device-resident state"},
-        "gpu_launches": 3 * args.steps,  # write + decode + merge per step (region 1)
+        "gpu_launches": 2 * args.steps,  # write + decode per step (region 1)
         "clocks": clk,
     }
     if args.cpu_baseline:
