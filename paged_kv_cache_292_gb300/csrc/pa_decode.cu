@@ -453,48 +453,76 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   if (ticket != r1 - r0) return;
   __threadfence();  // every other partial is visible now
-  constexpr int DL = D / 32;  // output dims per lane
+  // Online pass over the partials, four query heads of this KV head at a
+  // time: lane l owns dims [l*DL, l*DL+DL) of each head.  The next partial's
+  // loads are issued before the current one is folded in.
+  constexpr int DL = D / 32;
+  constexpr int GM = 4;
   const int G = p.group, H = p.num_heads;
-  T* out = reinterpret_cast<T*>(p.out) + (size_t)seq * H * D;
-  for (int g = 0; g < G; ++g) {
-    const int h = kv_head * G + g;
-    float big_m = -INFINITY;
-    for (int rr = r0 + lane; rr <= r1; rr += 32) {
-      const int sl = rr == r0 ? slot0 : 0;
-      big_m = fmaxf(big_m, __ldcg(p.part_ml + (((size_t)rr * 2 + sl) * H + h) * 2));
-    }
-    big_m = warp_max_f(big_m);
-    float den = 0.f;
-    for (int rr = r0 + lane; rr <= r1; rr += 32) {
-      const int sl = rr == r0 ? slot0 : 0;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + ((size_t)rr * 2 + sl) * H + h);
-      den += exp2f(ml.x - big_m) * ml.y;
-    }
-    den = warp_sum_f(den);
-    float acc[DL];
+  for (int g0 = 0; g0 < G; g0 += GM) {
+    const int h0 = kv_head * G + g0;
+    const int gn = min(GM, G - g0);
+    float run_m[GM], run_l[GM], acc[GM][DL];
+    float nm[GM], nl[GM], no[GM][DL];
 #pragma unroll
-    for (int i = 0; i < DL; ++i) acc[i] = 0.f;
-#pragma unroll 4
-    for (int rr = r0; rr <= r1; ++rr) {
+    for (int g = 0; g < GM; ++g) {
+      run_m[g] = -INFINITY;
+      run_l[g] = 0.f;
+#pragma unroll
+      for (int i = 0; i < DL; ++i) acc[g][i] = 0.f;
+    }
+    auto load = [&](int rr) {
       const int sl = rr == r0 ? slot0 : 0;
-      const size_t base = ((size_t)rr * 2 + sl) * H + h;
-      const float wgt = exp2f(__ldcg(p.part_ml + base * 2) - big_m);
-      const float* po = p.part_o + base * D + lane * DL;
-      if constexpr (DL == 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
-        acc[0] += wgt * v.x;
-        acc[1] += wgt * v.y;
-        acc[2] += wgt * v.z;
-        acc[3] += wgt * v.w;
-      } else {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
-        acc[0] += wgt * v.x;
-        acc[1] += wgt * v.y;
+      const size_t base = ((size_t)rr * 2 + sl) * H + h0;
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        if (g < gn) {
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + g);
+          nm[g] = ml.x;
+          nl[g] = ml.y;
+          const float* po = p.part_o + (base + g) * D + lane * DL;
+          if constexpr (DL == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+            no[g][0] = v.x; no[g][1] = v.y; no[g][2] = v.z; no[g][3] = v.w;
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+            no[g][0] = v.x; no[g][1] = v.y;
+          }
+        }
+      }
+    };
+    load(r0);
+    for (int rr = r0; rr <= r1; ++rr) {
+      float cm[GM], cl[GM], co[GM][DL];
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        cm[g] = nm[g];
+        cl[g] = nl[g];
+#pragma unroll
+        for (int i = 0; i < DL; ++i) co[g][i] = no[g][i];
+      }
+      if (rr < r1) load(rr + 1);
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        if (g < gn) {
+          const float mnew = fmaxf(run_m[g], cm[g]);
+          const float a_old = exp2f(run_m[g] - mnew), a_new = exp2f(cm[g] - mnew);
+          run_m[g] = mnew;
+          run_l[g] = run_l[g] * a_old + cl[g] * a_new;
+#pragma unroll
+          for (int i = 0; i < DL; ++i) acc[g][i] = acc[g][i] * a_old + co[g][i] * a_new;
+        }
       }
     }
-    const float inv = 1.f / den;
+    T* out = reinterpret_cast<T*>(p.out) + ((size_t)seq * H + h0) * D + lane * DL;
 #pragma unroll
-    for (int i = 0; i < DL; ++i) out[(size_t)h * D + lane * DL + i] = T(acc[i] * inv);
+    for (int g = 0; g < GM; ++g) {
+      if (g < gn) {
+        const float inv = 1.f / run_l[g];
+#pragma unroll
+        for (int i = 0; i < DL; ++i) out[(size_t)g * D + i] = T(acc[g][i] * inv);
+      }
+    }
   }
   __syncwarp();
   if (lane == 0) *cnt = 0;  // leave the counter zeroed for the next call
@@ -749,21 +777,26 @@ namespace {
 struct Plan {
   int Hg, HG, R, stages, q_slots;
   uint32_t row_bytes, pitch, q_bytes, stage_bytes, smem;
-  size_t ws_prefix, ws_ml, ws_o, ws_total;
+  size_t ws_ml, ws_o, ws_partials, ws_counters, ws_total;
 };
 
+// Scratch layout: partial (m, l) and O at the start, then the merge tickets
+// (num_seqs * num_kv_heads int32).  In a caller's buffer the tickets occupy
+// its last bytes (rounded down to 256), so that buffers reused across batch
+// shapes keep tickets and partials apart.
 size_t workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_size, int R,
                         Plan* pl) {
-  const size_t prefix = align_up(sizeof(int32_t) * (size_t)num_seqs * num_kv_heads, 256);
   const size_t ml = align_up(sizeof(float) * (size_t)R * 2 * num_heads * 2, 256);
   const size_t o = align_up(sizeof(float) * (size_t)R * 2 * num_heads * head_size, 256);
+  const size_t cnt = align_up(sizeof(int32_t) * (size_t)num_seqs * num_kv_heads, 256);
   if (pl) {
-    pl->ws_prefix = 0;
-    pl->ws_ml = prefix;
-    pl->ws_o = prefix + ml;
-    pl->ws_total = prefix + ml + o;
+    pl->ws_ml = 0;
+    pl->ws_o = ml;
+    pl->ws_partials = ml + o;
+    pl->ws_counters = cnt;
+    pl->ws_total = ml + o + cnt;
   }
-  return prefix + ml + o;
+  return ml + o + cnt;
 }
 
 // KV heads one CTA stages per token row: the largest divisor of num_kv_heads
@@ -911,14 +944,20 @@ int decode_impl(void* out, const void* query, const void* k_cache, const void* v
   Plan pl{};
   rc = make_plan(num_seqs, num_heads, num_kv_heads, head_size, elt, num_ranges, dev, &pl);
   if (rc != PA_OK) return rc;
+  int32_t* counters = nullptr;
   if (workspace == nullptr) {
-    rc = library_workspace(pl.ws_total, &workspace);
+    rc = library_workspace(pl.ws_partials, &workspace);
+    if (rc != PA_OK) return rc;
+    rc = library_counters(pl.ws_counters, &counters);
     if (rc != PA_OK) return rc;
   } else {
     if (workspace_bytes < pl.ws_total)
       return fail(PA_ERR_WORKSPACE, "pa_decode: workspace of %zu bytes, %zu needed", workspace_bytes,
                   pl.ws_total);
     if (!aligned(workspace, 256)) return fail(PA_ERR_INVALID_ARG, "pa_decode: workspace not 256-byte aligned");
+    const size_t cnt_bytes = sizeof(int32_t) * (size_t)num_seqs * num_kv_heads;
+    counters = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) +
+                                          ((workspace_bytes - cnt_bytes) & ~(size_t)255));
   }
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   DecodeParams prm{};
@@ -928,7 +967,7 @@ int decode_impl(void* out, const void* query, const void* k_cache, const void* v
   prm.v_cache = v_cache;
   prm.block_tables = block_tables;
   prm.context_lens = context_lens;
-  prm.counters = reinterpret_cast<int32_t*>(ws + pl.ws_prefix);
+  prm.counters = counters;
   prm.part_ml = reinterpret_cast<float*>(ws + pl.ws_ml);
   prm.part_o = reinterpret_cast<float*>(ws + pl.ws_o);
   prm.error_flag = error_flag;

@@ -20,6 +20,8 @@ DeviceInfo g_info[kMaxDevices];
 bool g_info_valid[kMaxDevices] = {false};
 void* g_ws_ptr[kMaxDevices] = {nullptr};
 size_t g_ws_bytes[kMaxDevices] = {0};
+void* g_cnt_ptr[kMaxDevices] = {nullptr};
+size_t g_cnt_bytes[kMaxDevices] = {0};
 }  // namespace
 
 int fail(int code, const char* fmt, ...) {
@@ -80,14 +82,39 @@ int library_workspace(size_t bytes, void** ptr) {
       g_ws_ptr[dev] = nullptr;
       return cuda_fail(e, "cudaMalloc(workspace)");
     }
-    // Decode's merge tickets must start at zero; every completed call leaves
-    // them zero again.
-    e = cudaMemset(g_ws_ptr[dev], 0, want);
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
     g_ws_bytes[dev] = want;
   }
   *ptr = g_ws_ptr[dev];
+  return PA_OK;
+}
+
+int library_counters(size_t bytes, int32_t** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_cnt_bytes[dev] < bytes) {
+    if (g_cnt_ptr[dev] != nullptr) {
+      e = cudaFree(g_cnt_ptr[dev]);
+      g_cnt_ptr[dev] = nullptr;
+      g_cnt_bytes[dev] = 0;
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFree(tickets)");
+    }
+    const size_t want = align_up(bytes < 65536 ? 65536 : bytes, 65536);
+    void* p = nullptr;
+    e = cudaMalloc(&p, want);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(tickets)");
+    // Merge tickets start at zero; every completed decode leaves them zero.
+    e = cudaMemset(p, 0, want);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      cudaFree(p);
+      return cuda_fail(e, "cudaMemset(tickets)");
+    }
+    g_cnt_ptr[dev] = p;
+    g_cnt_bytes[dev] = want;
+  }
+  *ptr = static_cast<int32_t*>(g_cnt_ptr[dev]);
   return PA_OK;
 }
 

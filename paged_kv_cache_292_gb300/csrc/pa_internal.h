@@ -27,6 +27,10 @@ int current_device_info(DeviceInfo* info);
 // Growing frees the old buffer (cudaFree synchronises the device).
 int library_workspace(size_t bytes, void** ptr);
 
+// Library-owned, zero-filled merge-ticket buffer for the current device, grown
+// to at least `bytes` (zero-filled again when it grows).
+int library_counters(size_t bytes, int32_t** ptr);
+
 inline bool aligned(const void* p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

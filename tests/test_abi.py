@@ -97,7 +97,7 @@ def test_workspace_size_formula(lib):
         return (x + 255) // 256 * 256
 
     S, H, Hk, D, R = 64, 32, 8, 128, 100
-    want = up(4 * S * Hk) + up(4 * R * 2 * H * 2) + up(4 * R * 2 * H * D)
+    want = up(4 * R * 2 * H * 2) + up(4 * R * 2 * H * D) + up(4 * S * Hk)
     assert lib.pa_decode_workspace_size(S, H, Hk, D, R) == want
     assert lib.pa_decode_workspace_size(0, H, Hk, D, R) == 0
     assert lib.pa_decode_workspace_size(S, 12, 8, D, R) == 0
