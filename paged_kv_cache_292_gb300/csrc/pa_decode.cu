@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   int* abort_flag = reinterpret_cast<int*>(misc + 34);
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(full_bar(i), 1);
+      mbar_init(full_bar(i), 2);  // producer: expect_tx arrival + metadata arrival
       mbar_init(empty_bar(i), Hg);
     }
     for (int i = 0; i < NQ; ++i) {
@@ -650,11 +650,6 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const int blk0 = tok0 / bs;
       if (new_seq) {
         slot = segment_slot(a, b, ps, ps + ns);
-        if (slot >= 0) {
-          seg_r0 = static_cast<int>(range_of_tile(ps, total, Reff));
-          seg_r1 = static_cast<int>(range_of_tile(ps + ns - 1, total, Reff));
-          seg_slot0 = partial_slot_of_range(seg_r0, ps, total, Reff);
-        }
         bt_row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
         nblk = (c + bs - 1) / bs;
         cb = blk0;
@@ -666,8 +661,6 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         cb += 32;
         nxt = table_entry(cb + 32 + lane);
       }
-      const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
-                        ((slot + 1) << 2) | (seg_slot0 << 4);
       if (new_seq) {
         if (!mbar_wait(qempty_bar(qi), qph ^ 1u)) {
           report(p.error_flag, PA_DEVERR_TIMEOUT);
@@ -701,16 +694,27 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         report(p.error_flag, PA_DEVERR_TIMEOUT);
         break;
       }
-      if (lane == 0) {
-        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, 0, 0};
-        mbar_arrive_expect_tx(full_bar(st), __popc(copies) * p.row_bytes);
-      }
+      if (lane == 0) mbar_arrive_expect_tx(full_bar(st), __popc(copies) * p.row_bytes);
       __syncwarp();
       if (ok) {
         const size_t row = ((size_t)phys * bs + tok % bs) * Hk + (size_t)hg * Hg;
         const T* src = (is_v ? vc : kc) + row * D;
         const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
         bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
+      }
+      // The stage's metadata goes out after its copies are in flight: the
+      // merge bookkeeping of a cut sequence (64-bit range arithmetic) stays off
+      // the path to the first bytes.  The second arrival publishes it.
+      if (new_seq && slot >= 0) {
+        seg_r0 = static_cast<int>(range_of_tile(ps, total, Reff));
+        seg_r1 = static_cast<int>(range_of_tile(ps + ns - 1, total, Reff));
+        seg_slot0 = partial_slot_of_range(seg_r0, ps, total, Reff);
+      }
+      if (lane == 0) {
+        const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
+                          ((slot + 1) << 2) | (seg_slot0 << 4);
+        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, 0, 0};
+        mbar_arrive(full_bar(st));
       }
       if (++st == NS) {
         st = 0;

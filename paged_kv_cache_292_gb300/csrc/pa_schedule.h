@@ -28,12 +28,19 @@ namespace pa {
 constexpr int kTile = 16;  // tokens per tile (one MMA M-extent, one pipeline stage)
 
 PA_HD int64_t range_start(int64_t r, int64_t total_tiles, int64_t num_ranges) {
-  return (r * total_tiles) / num_ranges;
+  const int64_t prod = r * total_tiles;
+  // 32-bit division when the operands fit (the common case; much cheaper on the GPU).
+  if (prod < (int64_t(1) << 32) && num_ranges < (int64_t(1) << 32))
+    return static_cast<int64_t>(static_cast<uint32_t>(prod) / static_cast<uint32_t>(num_ranges));
+  return prod / num_ranges;
 }
 
 // The range that owns tile x (0 <= x < total_tiles).  Empty ranges own nothing.
 PA_HD int64_t range_of_tile(int64_t x, int64_t total_tiles, int64_t num_ranges) {
-  int64_t r = (x * num_ranges) / total_tiles;
+  const int64_t prod = x * num_ranges;
+  int64_t r = (prod < (int64_t(1) << 32) && total_tiles < (int64_t(1) << 32))
+                  ? static_cast<int64_t>(static_cast<uint32_t>(prod) / static_cast<uint32_t>(total_tiles))
+                  : prod / total_tiles;
   if (r >= num_ranges) r = num_ranges - 1;
   while (r + 1 < num_ranges && range_start(r + 1, total_tiles, num_ranges) <= x) ++r;
   while (r > 0 && range_start(r, total_tiles, num_ranges) > x) --r;
