@@ -453,17 +453,17 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   if (ticket != r1 - r0) return;
   __threadfence();  // every other partial is visible now
-  // Online pass over the partials, four query heads of this KV head at a
-  // time: lane l owns dims [l*DL, l*DL+DL) of each head.  The next partial's
-  // loads are issued before the current one is folded in.
+  // Online log-sum-exp over the partials, two query heads of this KV head at a
+  // time; lane l owns dims [l*DL, l*DL+DL) of each head.  The loads of up to
+  // four partials are issued together, so a cut sequence's merge costs about
+  // one L2 round trip per four partials.
   constexpr int DL = D / 32;
-  constexpr int GM = 4;
+  constexpr int GM = 2, PB = 4;
   const int G = p.group, H = p.num_heads;
   for (int g0 = 0; g0 < G; g0 += GM) {
     const int h0 = kv_head * G + g0;
     const int gn = min(GM, G - g0);
     float run_m[GM], run_l[GM], acc[GM][DL];
-    float nm[GM], nl[GM], no[GM][DL];
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
       run_m[g] = -INFINITY;
@@ -471,47 +471,52 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 #pragma unroll
       for (int i = 0; i < DL; ++i) acc[g][i] = 0.f;
     }
-    auto load = [&](int rr) {
-      const int sl = rr == r0 ? slot0 : 0;
-      const size_t base = ((size_t)rr * 2 + sl) * H + h0;
+    for (int rb = r0; rb <= r1; rb += PB) {
+      float bm[PB][GM], bl[PB][GM], bo[PB][GM][DL];
 #pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        if (g < gn) {
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + g);
-          nm[g] = ml.x;
-          nl[g] = ml.y;
-          const float* po = p.part_o + (base + g) * D + lane * DL;
-          if constexpr (DL == 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
-            no[g][0] = v.x; no[g][1] = v.y; no[g][2] = v.z; no[g][3] = v.w;
+      for (int k = 0; k < PB; ++k) {
+        const int rr = rb + k;
+        const int sl = rr == r0 ? slot0 : 0;
+        const size_t base = ((size_t)rr * 2 + sl) * H + h0;
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+          if (rr <= r1 && g < gn) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + g);
+            bm[k][g] = ml.x;
+            bl[k][g] = ml.y;
+            const float* po = p.part_o + (base + g) * D + lane * DL;
+            if constexpr (DL == 4) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+              bo[k][g][0] = v.x; bo[k][g][1] = v.y; bo[k][g][2] = v.z; bo[k][g][3] = v.w;
+            } else {
+              const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+              bo[k][g][0] = v.x; bo[k][g][1] = v.y;
+            }
           } else {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
-            no[g][0] = v.x; no[g][1] = v.y;
+            bm[k][g] = -INFINITY;
+            bl[k][g] = 0.f;
+#pragma unroll
+            for (int i = 0; i < DL; ++i) bo[k][g][i] = 0.f;
           }
         }
       }
-    };
-    load(r0);
-    for (int rr = r0; rr <= r1; ++rr) {
-      float cm[GM], cl[GM], co[GM][DL];
 #pragma unroll
       for (int g = 0; g < GM; ++g) {
-        cm[g] = nm[g];
-        cl[g] = nl[g];
+        float mnew = run_m[g];
 #pragma unroll
-        for (int i = 0; i < DL; ++i) co[g][i] = no[g][i];
-      }
-      if (rr < r1) load(rr + 1);
+        for (int k = 0; k < PB; ++k) mnew = fmaxf(mnew, bm[k][g]);
+        const float a_old = exp2f(run_m[g] - mnew);  // run_m = -inf on the first batch: 0
+        run_l[g] *= a_old;
 #pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        if (g < gn) {
-          const float mnew = fmaxf(run_m[g], cm[g]);
-          const float a_old = exp2f(run_m[g] - mnew), a_new = exp2f(cm[g] - mnew);
-          run_m[g] = mnew;
-          run_l[g] = run_l[g] * a_old + cl[g] * a_new;
+        for (int i = 0; i < DL; ++i) acc[g][i] *= a_old;
 #pragma unroll
-          for (int i = 0; i < DL; ++i) acc[g][i] = acc[g][i] * a_old + co[g][i] * a_new;
+        for (int k = 0; k < PB; ++k) {
+          const float wk = exp2f(bm[k][g] - mnew);  // 0 for padding entries
+          run_l[g] += wk * bl[k][g];
+#pragma unroll
+          for (int i = 0; i < DL; ++i) acc[g][i] += wk * bo[k][g][i];
         }
+        run_m[g] = mnew;
       }
     }
     T* out = reinterpret_cast<T*>(p.out) + ((size_t)seq * H + h0) * D + lane * DL;
