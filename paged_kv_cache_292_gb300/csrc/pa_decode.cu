@@ -453,12 +453,12 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   if (ticket != r1 - r0) return;
   __threadfence();  // every other partial is visible now
-  // Online log-sum-exp over the partials, two query heads of this KV head at a
+  // Online log-sum-exp over the partials, four query heads of this KV head at a
   // time; lane l owns dims [l*DL, l*DL+DL) of each head.  The loads of up to
   // four partials are issued together, so a cut sequence's merge costs about
   // one L2 round trip per four partials.
   constexpr int DL = D / 32;
-  constexpr int GM = 2, PB = 4;
+  constexpr int GM = 4, PB = 4;
   const int G = p.group, H = p.num_heads;
   for (int g0 = 0; g0 < G; g0 += GM) {
     const int h0 = kv_head * G + g0;
