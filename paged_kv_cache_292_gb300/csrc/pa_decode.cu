@@ -547,14 +547,21 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const int Hg = p.heads_per_cta;
   const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes);
   long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
-  griddep_wait();  // inputs may come from the kernel just before (e.g. the cache write)
+  // Programmatic dependent launch: this grid may start while the kernel before
+  // it on the stream (e.g. the cache write) is still running.  The prologue and
+  // the block-table reads below only touch context_lens and block_tables, which
+  // such an early-triggering predecessor must not write; everything else (query,
+  // pools, output, scratch) is touched only after griddep_wait().
 
   // ---- Prologue: total tile count, this range, and its first sequence. ----
   long long total = 0;
   for (int base = 0; base < S; base += nthreads) {
     const int s = base + tid;
     long long n = (s < S) ? tiles_of(clamp_context(p, s, true)) : 0;
-    if (s < S && n == 0 && s % gridDim.x == blockIdx.x) zero_row<T, D>(p, s);
+    if (s < S && n == 0 && s % gridDim.x == blockIdx.x) {
+      griddep_wait();
+      zero_row<T, D>(p, s);
+    }
     n = warp_sum_ll(n);
     if (lane == 0) misc[warp] = n;
     __syncthreads();
@@ -666,6 +673,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         cb += 32;
         nxt = table_entry(cb + 32 + lane);
       }
+      if (x == a) griddep_wait();  // first touch of query and pools
       if (new_seq) {
         if (!mbar_wait(qempty_bar(qi), qph ^ 1u)) {
           report(p.error_flag, PA_DEVERR_TIMEOUT);
