@@ -473,30 +473,27 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
     }
     for (int rb = r0; rb <= r1; rb += PB) {
       float bm[PB][GM], bl[PB][GM], bo[PB][GM][DL];
+      // Unconditional loads (indices clamped to valid partials and heads) so
+      // that all of them are in flight together; padding gets weight zero.
 #pragma unroll
       for (int k = 0; k < PB; ++k) {
-        const int rr = rb + k;
+        const int rr = min(rb + k, r1);
         const int sl = rr == r0 ? slot0 : 0;
         const size_t base = ((size_t)rr * 2 + sl) * H + h0;
 #pragma unroll
         for (int g = 0; g < GM; ++g) {
-          if (rr <= r1 && g < gn) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + g);
-            bm[k][g] = ml.x;
-            bl[k][g] = ml.y;
-            const float* po = p.part_o + (base + g) * D + lane * DL;
-            if constexpr (DL == 4) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
-              bo[k][g][0] = v.x; bo[k][g][1] = v.y; bo[k][g][2] = v.z; bo[k][g][3] = v.w;
-            } else {
-              const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
-              bo[k][g][0] = v.x; bo[k][g][1] = v.y;
-            }
+          const int gc = min(g, gn - 1);
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + gc);
+          const bool real = (rb + k <= r1) && (g < gn);
+          bm[k][g] = real ? ml.x : -INFINITY;
+          bl[k][g] = real ? ml.y : 0.f;
+          const float* po = p.part_o + (base + gc) * D + lane * DL;
+          if constexpr (DL == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+            bo[k][g][0] = v.x; bo[k][g][1] = v.y; bo[k][g][2] = v.z; bo[k][g][3] = v.w;
           } else {
-            bm[k][g] = -INFINITY;
-            bl[k][g] = 0.f;
-#pragma unroll
-            for (int i = 0; i < DL; ++i) bo[k][g][i] = 0.f;
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+            bo[k][g][0] = v.x; bo[k][g][1] = v.y;
           }
         }
       }
