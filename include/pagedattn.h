@@ -157,6 +157,34 @@ int pa_write_cache_ex(const void* k_new, const void* v_new, const int64_t* slot_
                       int head_size, int block_size, int num_physical_blocks, void* stream,
                       int dtype, int32_t* error_flag);
 
+/*
+ * pa_decode_static - pa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc when they decode, e.g. a serving engine whose
+ * own allocator has already reserved nearly all device memory, or a latency
+ * path that cannot afford cudaMalloc's implicit device synchronisation.
+ * Arguments, layouts and results are those of pa_decode.  Instead of
+ * allocating scratch it uses an array of PA_STATIC_SCRATCH_BYTES compiled
+ * into the library: every GPU that loads the library holds that memory until
+ * the process exits.  Nothing is allocated or freed by this call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the previous call's
+ *     contents; each call clears the part that must start at zero (with
+ *     cudaMemsetAsync on `stream`) before its kernel.  Calls that overlap in
+ *     time on the GPU (different streams, no ordering) race on the array.
+ *   - Batches whose scratch (pa_decode_workspace_size(num_seqs, num_heads,
+ *     num_kv_heads, head_size, 0)) exceeds PA_STATIC_SCRATCH_BYTES are
+ *     rejected with PA_ERR_WORKSPACE before anything is launched.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int pa_decode_static(void* out, const void* query, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                     int num_heads, int num_kv_heads, int head_size, int block_size,
+                     int max_blocks_per_seq, float scale, void* stream, int dtype);
+
 /* Message for the calling thread's last non-zero return ("" if none). */
 const char* pa_last_error(void);
 

@@ -52,6 +52,7 @@ _SIGS = {
         [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _I, _I, _P, _SZ, _I, _P],
     ),
     "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "pa_decode_static": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _I]),
     "pa_write_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I]),
     "pa_write_cache_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P]),
     "pa_last_error": (ctypes.c_char_p, []),
@@ -146,6 +147,15 @@ def pa_decode_ex(out, query, k_cache, v_cache, block_tables, context_lens, num_s
                                _ptr(context_lens), num_seqs, num_heads, num_kv_heads, head_size, block_size,
                                max_blocks_per_seq, scale, _stream(stream), dtype, num_physical_blocks,
                                _ptr(workspace), workspace_bytes, num_ranges, _ptr(error_flag)))
+
+
+def pa_decode_static(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads, num_kv_heads,
+                     head_size, block_size, max_blocks_per_seq, scale, stream=None, dtype=None):
+    """pa_decode without any allocation: scratch is an array compiled into the library."""
+    dtype = dtype_code(query.dtype) if dtype is None else dtype
+    _check(load().pa_decode_static(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                   _ptr(context_lens), num_seqs, num_heads, num_kv_heads, head_size, block_size,
+                                   max_blocks_per_seq, scale, _stream(stream), dtype))
 
 
 def pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, num_ranges=0) -> int:

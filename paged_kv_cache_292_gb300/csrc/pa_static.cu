@@ -1,0 +1,90 @@
+// pa_decode_static: paged decode that allocates nothing.
+//
+// Some callers cannot call cudaMalloc at the point where they decode: a
+// serving engine whose own allocator has already reserved nearly all device
+// memory (a fresh cudaMalloc then fails or fragments its pool), or a latency
+// path that cannot afford cudaMalloc/cudaFree's implicit device
+// synchronisation.  pa_decode allocates its scratch on first use and
+// pa_decode_ws needs the caller to provide some; this entry point instead uses
+// a fixed scratch array compiled into the library.  The caller still passes
+// every input and output buffer.
+//
+// The array is a file-scope __device__ variable, so every GPU that loads this
+// library holds PA_STATIC_SCRATCH_BYTES of it until the process exits.  In
+// host code its name is only a host-side stand-in, not a device address; the
+// device address is fetched once per device with cudaGetSymbolAddress, with
+// that device current, on the first call made on that device.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/pagedattn.h"
+#include "pa_internal.h"
+
+static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_SCRATCH_BYTES];
+
+namespace pa {
+
+int decode_impl(void* out, const void* query, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                int num_heads, int num_kv_heads, int head_size, int block_size,
+                int max_blocks_per_seq, float scale, void* stream, int dtype,
+                int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                int32_t* error_flag);
+size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                             int num_ranges);
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mutex;
+void* g_static_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device (set up once per
+// device, with that device current).
+int static_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device index %d too large", dev);
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
+  return PA_OK;
+}
+}  // namespace
+
+}  // namespace pa
+
+extern "C" int pa_decode_static(void* out, const void* query, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                const int32_t* context_lens, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_size, int block_size,
+                                int max_blocks_per_seq, float scale, void* stream, int dtype) {
+  pa::clear_error();
+  const size_t need = pa::decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, 0);
+  if (need == 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_static: invalid sizes (or no usable device)");
+  if (need > (size_t)PA_STATIC_SCRATCH_BYTES)
+    return pa::fail(PA_ERR_WORKSPACE,
+                    "pa_decode_static: this batch needs %zu bytes of scratch, more than the %zu "
+                    "compiled in (use pa_decode or pa_decode_ws)",
+                    need, (size_t)PA_STATIC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  int rc = pa::static_scratch(&scratch);
+  if (rc != PA_OK) return rc;
+  // The merge tickets (in the scratch's last bytes for this batch shape) must
+  // start at zero; the array keeps whatever the previous call left, so clear
+  // them on the caller's stream first.
+  const size_t tickets = pa::align_up(sizeof(int32_t) * (size_t)num_seqs * num_kv_heads, 256);
+  cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - tickets), 0,
+                                  tickets, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return pa::cuda_fail(e, "cudaMemsetAsync(static scratch tickets)");
+  return pa::decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                         num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                         stream, dtype, 0, scratch, need, 0, nullptr);
+}
