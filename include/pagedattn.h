@@ -35,12 +35,10 @@
  *     slot outside the pool) are reported by OR-ing PA_DEVERR_* bits into the
  *     optional device word `error_flag`; the offending row is skipped (its
  *     content is then unspecified) instead of being read or written.
- *   - Kernels are launched with programmatic stream serialisation.  If the
- *     kernel just before a pa_decode call on the stream triggers programmatic
- *     launch completion early (griddepcontrol.launch_dependents, as
- *     pa_write_cache does), it must not write block_tables or context_lens:
- *     pa_decode reads those two before waiting for it.  Everything else is
- *     touched only after that kernel has completed.
+ *   - Kernels are launched with programmatic stream serialisation: a kernel
+ *     may become resident while the one before it on the stream finishes, but
+ *     it reads and writes nothing until that kernel has completed
+ *     (griddepcontrol.wait).
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H

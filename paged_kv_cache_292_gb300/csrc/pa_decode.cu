@@ -453,17 +453,17 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   if (ticket != r1 - r0) return;
   __threadfence();  // every other partial is visible now
-  // Online log-sum-exp over the partials, four query heads of this KV head at a
-  // time; lane l owns dims [l*DL, l*DL+DL) of each head.  The loads of up to
-  // four partials are issued together, so a cut sequence's merge costs about
-  // one L2 round trip per four partials.
+  // Online pass over the partials, four query heads of this KV head at a
+  // time: lane l owns dims [l*DL, l*DL+DL) of each head.  The next partial's
+  // loads are issued before the current one is folded in.
   constexpr int DL = D / 32;
-  constexpr int GM = 4, PB = 4;
+  constexpr int GM = 4;
   const int G = p.group, H = p.num_heads;
   for (int g0 = 0; g0 < G; g0 += GM) {
     const int h0 = kv_head * G + g0;
     const int gn = min(GM, G - g0);
     float run_m[GM], run_l[GM], acc[GM][DL];
+    float nm[GM], nl[GM], no[GM][DL];
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
       run_m[g] = -INFINITY;
@@ -471,49 +471,47 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 #pragma unroll
       for (int i = 0; i < DL; ++i) acc[g][i] = 0.f;
     }
-    for (int rb = r0; rb <= r1; rb += PB) {
-      float bm[PB][GM], bl[PB][GM], bo[PB][GM][DL];
-      // Unconditional loads (indices clamped to valid partials and heads) so
-      // that all of them are in flight together; padding gets weight zero.
+    auto load = [&](int rr) {
+      const int sl = rr == r0 ? slot0 : 0;
+      const size_t base = ((size_t)rr * 2 + sl) * H + h0;
 #pragma unroll
-      for (int k = 0; k < PB; ++k) {
-        const int rr = min(rb + k, r1);
-        const int sl = rr == r0 ? slot0 : 0;
-        const size_t base = ((size_t)rr * 2 + sl) * H + h0;
-#pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          const int gc = min(g, gn - 1);
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + gc);
-          const bool real = (rb + k <= r1) && (g < gn);
-          bm[k][g] = real ? ml.x : -INFINITY;
-          bl[k][g] = real ? ml.y : 0.f;
-          const float* po = p.part_o + (base + gc) * D + lane * DL;
+      for (int g = 0; g < GM; ++g) {
+        if (g < gn) {
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + base + g);
+          nm[g] = ml.x;
+          nl[g] = ml.y;
+          const float* po = p.part_o + (base + g) * D + lane * DL;
           if constexpr (DL == 4) {
             const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
-            bo[k][g][0] = v.x; bo[k][g][1] = v.y; bo[k][g][2] = v.z; bo[k][g][3] = v.w;
+            no[g][0] = v.x; no[g][1] = v.y; no[g][2] = v.z; no[g][3] = v.w;
           } else {
             const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
-            bo[k][g][0] = v.x; bo[k][g][1] = v.y;
+            no[g][0] = v.x; no[g][1] = v.y;
           }
         }
       }
+    };
+    load(r0);
+    for (int rr = r0; rr <= r1; ++rr) {
+      float cm[GM], cl[GM], co[GM][DL];
 #pragma unroll
       for (int g = 0; g < GM; ++g) {
-        float mnew = run_m[g];
+        cm[g] = nm[g];
+        cl[g] = nl[g];
 #pragma unroll
-        for (int k = 0; k < PB; ++k) mnew = fmaxf(mnew, bm[k][g]);
-        const float a_old = exp2f(run_m[g] - mnew);  // run_m = -inf on the first batch: 0
-        run_l[g] *= a_old;
+        for (int i = 0; i < DL; ++i) co[g][i] = no[g][i];
+      }
+      if (rr < r1) load(rr + 1);
 #pragma unroll
-        for (int i = 0; i < DL; ++i) acc[g][i] *= a_old;
+      for (int g = 0; g < GM; ++g) {
+        if (g < gn) {
+          const float mnew = fmaxf(run_m[g], cm[g]);
+          const float a_old = exp2f(run_m[g] - mnew), a_new = exp2f(cm[g] - mnew);
+          run_m[g] = mnew;
+          run_l[g] = run_l[g] * a_old + cl[g] * a_new;
 #pragma unroll
-        for (int k = 0; k < PB; ++k) {
-          const float wk = exp2f(bm[k][g] - mnew);  // 0 for padding entries
-          run_l[g] += wk * bl[k][g];
-#pragma unroll
-          for (int i = 0; i < DL; ++i) acc[g][i] += wk * bo[k][g][i];
+          for (int i = 0; i < DL; ++i) acc[g][i] = acc[g][i] * a_old + co[g][i] * a_new;
         }
-        run_m[g] = mnew;
       }
     }
     T* out = reinterpret_cast<T*>(p.out) + ((size_t)seq * H + h0) * D + lane * DL;
@@ -544,21 +542,14 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const int Hg = p.heads_per_cta;
   const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes);
   long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
-  // Programmatic dependent launch: this grid may start while the kernel before
-  // it on the stream (e.g. the cache write) is still running.  The prologue and
-  // the block-table reads below only touch context_lens and block_tables, which
-  // such an early-triggering predecessor must not write; everything else (query,
-  // pools, output, scratch) is touched only after griddep_wait().
+  griddep_wait();  // inputs may come from the kernel just before (e.g. the cache write)
 
   // ---- Prologue: total tile count, this range, and its first sequence. ----
   long long total = 0;
   for (int base = 0; base < S; base += nthreads) {
     const int s = base + tid;
     long long n = (s < S) ? tiles_of(clamp_context(p, s, true)) : 0;
-    if (s < S && n == 0 && s % gridDim.x == blockIdx.x) {
-      griddep_wait();
-      zero_row<T, D>(p, s);
-    }
+    if (s < S && n == 0 && s % gridDim.x == blockIdx.x) zero_row<T, D>(p, s);
     n = warp_sum_ll(n);
     if (lane == 0) misc[warp] = n;
     __syncthreads();
@@ -602,7 +593,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   int* abort_flag = reinterpret_cast<int*>(misc + 34);
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(full_bar(i), 2);  // producer: expect_tx arrival + metadata arrival
+      mbar_init(full_bar(i), 1);
       mbar_init(empty_bar(i), Hg);
     }
     for (int i = 0; i < NQ; ++i) {
@@ -659,6 +650,11 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const int blk0 = tok0 / bs;
       if (new_seq) {
         slot = segment_slot(a, b, ps, ps + ns);
+        if (slot >= 0) {
+          seg_r0 = static_cast<int>(range_of_tile(ps, total, Reff));
+          seg_r1 = static_cast<int>(range_of_tile(ps + ns - 1, total, Reff));
+          seg_slot0 = partial_slot_of_range(seg_r0, ps, total, Reff);
+        }
         bt_row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
         nblk = (c + bs - 1) / bs;
         cb = blk0;
@@ -670,7 +666,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         cb += 32;
         nxt = table_entry(cb + 32 + lane);
       }
-      if (x == a) griddep_wait();  // first touch of query and pools
+      const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
+                        ((slot + 1) << 2) | (seg_slot0 << 4);
       if (new_seq) {
         if (!mbar_wait(qempty_bar(qi), qph ^ 1u)) {
           report(p.error_flag, PA_DEVERR_TIMEOUT);
@@ -704,27 +701,16 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         report(p.error_flag, PA_DEVERR_TIMEOUT);
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(full_bar(st), __popc(copies) * p.row_bytes);
+      if (lane == 0) {
+        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, 0, 0};
+        mbar_arrive_expect_tx(full_bar(st), __popc(copies) * p.row_bytes);
+      }
       __syncwarp();
       if (ok) {
         const size_t row = ((size_t)phys * bs + tok % bs) * Hk + (size_t)hg * Hg;
         const T* src = (is_v ? vc : kc) + row * D;
         const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
         bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
-      }
-      // The stage's metadata goes out after its copies are in flight: the
-      // merge bookkeeping of a cut sequence (64-bit range arithmetic) stays off
-      // the path to the first bytes.  The second arrival publishes it.
-      if (new_seq && slot >= 0) {
-        seg_r0 = static_cast<int>(range_of_tile(ps, total, Reff));
-        seg_r1 = static_cast<int>(range_of_tile(ps + ns - 1, total, Reff));
-        seg_slot0 = partial_slot_of_range(seg_r0, ps, total, Reff);
-      }
-      if (lane == 0) {
-        const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
-                          ((slot + 1) << 2) | (seg_slot0 << 4);
-        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, 0, 0};
-        mbar_arrive(full_bar(st));
       }
       if (++st == NS) {
         st = 0;
