@@ -147,6 +147,20 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time: the whole job is done only when every replica is."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(step_bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank runs its own replica, so the job moves world x the bytes."""
+    return world * step_bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def make_replica(name: str, rank: int):
     spec_name, bs = WORKLOADS[name]
     sp = workloads.spec(spec_name)
@@ -335,12 +349,9 @@ def run_ours(args):
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     dec_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_step = total_ms / args.steps
-    value = world * by["step"] / (ms_step * 1e-3) / 1e9
+    value = job_throughput(by["step"], world, ms_step)
 
     # ---- end to end through the public API, host buffers ----
     host = {k: getattr(w, k).pin_memory() for k in ("q", "block_tables", "context_lens", "slot_mapping", "k_new",
@@ -369,11 +380,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * by["step"] / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = job_throughput(by["step"], world, e2e_ms)
 
     if rank != 0:
         if world > 1:
