@@ -161,8 +161,9 @@ def job_throughput(step_bytes_per_rank: int, world: int, ms_per_step: float) -> 
     return world * step_bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
-def make_replica(name: str, rank: int):
+def make_replica(name: str, rank: int, block_size=None):
     spec_name, bs = WORKLOADS[name]
+    bs = block_size or bs
     sp = workloads.spec(spec_name)
     if rank:
         sp = workloads.dataclasses.replace(sp, seed=sp.seed + 1000 * rank)
@@ -287,7 +288,7 @@ def run_ours(args):
     pa_build.build()
     lib = binding.load()
 
-    w = make_replica(args.workload, rank)
+    w = make_replica(args.workload, rank, args.block_size)
     sp = w.spec
     by = step_bytes(w)
     S, H, D = w.q.shape
@@ -302,13 +303,13 @@ def run_ours(args):
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # merge tickets start at zero
     P = binding._ptr
 
-    def write(gg):
+    def write(gg, sh=sh):
         rc = lib.pa_write_cache(P(gg["k_new"]), P(gg["v_new"]), P(gg["slot_mapping"]), P(g["k_cache"]),
                                 P(g["v_cache"]), S, Hk, D, bs, NB, sh, dt)
         if rc:
             raise RuntimeError(binding.pa_last_error())
 
-    def decode(gg, o):
+    def decode(gg, o, sh=sh):
         rc = lib.pa_decode_ws(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
                               P(gg["context_lens"]), S, H, Hk, D, bs, MB, w.scale, sh, dt, P(ws), ws_bytes)
         if rc:
@@ -330,10 +331,23 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     # Timed region 1: K whole steps back to back (the step's kernels are
     # chained with programmatic dependent launch, so no events in between).
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)  # capture needs a stream other than the legacy default
+        with torch.cuda.graph(graph, stream=cap):
+            write(g, cap.cuda_stream)
+            decode(g, out, cap.cuda_stream)
+        torch.cuda.synchronize(dev)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(dev)
     t_start.record(stream)
     for _ in range(args.steps):
-        write(g)
-        decode(g, out)
+        if args.graph:
+            graph.replay()
+        else:
+            write(g)
+            decode(g, out)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     # Timed region 2: the same K steps with events around each pa_decode call
@@ -414,6 +428,7 @@ def run_ours(args):
             "l2": f"inputs larger than L2: {by['kv_logical'] / 1e9:.3f} GB of K/V read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
             "replicas": world,
+            "launch": "CUDA graph replay" if args.graph else "eager (programmatic dependent launch)",
         },
         "roofline": {
             "kernel": "pa_decode_kernel (one launch per pa_decode call; split sequences merged in-kernel)",
@@ -452,6 +467,9 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOADS), default="llama3_8b")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of the step captured in a CUDA graph (region 1) instead of eager calls")
+    ap.add_argument("--block-size", type=int, default=None, help="override the workload's block size")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
