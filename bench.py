@@ -19,6 +19,8 @@ on the data path); the max time over ranks is used and `value` sums all ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
+import math
 import hashlib
 import json
 import os
@@ -458,6 +460,109 @@ def run_ours(args):
     return 0
 
 
+def run_loop(args):
+    """Steady-state decode driven by the host block manager, K steps.
+
+    Each step: one batched pa_bm_append (one new token per sequence, blocks
+    allocated on demand), export of block tables and lengths into pinned host
+    buffers, their host-to-device copy, the cache write and the decode.  The
+    timed region covers the host work too (wall clock, synchronised at both
+    ends)."""
+    from paged_kv_cache_292_gb300 import binding
+    from paged_kv_cache_292_gb300 import build as pa_build
+
+    pa_build.build()
+    lib = binding.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    spec_name, bs0 = WORKLOADS[args.workload]
+    sp = workloads.spec(spec_name)
+    bs = args.block_size or bs0 or sp.block_size
+    S, H, Hk, D = sp.num_seqs, sp.num_heads, sp.num_kv_heads, sp.head_size
+    ctx0 = workloads._draw_context_lens(dataclasses_replace(sp, block_size=bs))
+    steps = args.steps
+    mb = -(-(int(ctx0.max()) + steps + args.warmup + 1) // bs)
+    nb = int(sum(-(-(int(c) + steps + args.warmup + 1) // bs) for c in ctx0)) + S
+    tdt = torch.bfloat16 if sp.dtype == "bf16" else torch.float32
+    gen = torch.Generator(device=dev).manual_seed(sp.seed)
+    k_cache = torch.randn((nb, bs, Hk, D), generator=gen, device=dev).to(tdt)
+    v_cache = torch.randn((nb, bs, Hk, D), generator=gen, device=dev).to(tdt)
+    q = torch.randn((S, H, D), generator=gen, device=dev).to(tdt)
+    k_new = torch.randn((S, Hk, D), generator=gen, device=dev).to(tdt)
+    v_new = torch.randn((S, Hk, D), generator=gen, device=dev).to(tdt)
+    bm = binding.BlockManager(nb, bs, S, mb)
+    for s_, c in enumerate(ctx0.tolist()):
+        bm.append(s_, c - 1)  # the prompt's K/V already sits in the (random) pool
+    seqs = torch.arange(S, dtype=torch.int32)
+    ones = torch.ones(S, dtype=torch.int32)
+    slots_h = torch.empty(S, dtype=torch.int64).pin_memory()
+    copies_h = torch.empty(2 * S, dtype=torch.int32)
+    tables_h = torch.empty((S, mb), dtype=torch.int32).pin_memory()
+    lens_h = torch.empty(S, dtype=torch.int32).pin_memory()
+    slots_d = torch.empty(S, dtype=torch.int64, device=dev)
+    tables_d = torch.empty((S, mb), dtype=torch.int32, device=dev)
+    lens_d = torch.empty(S, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    ws_bytes = lib.pa_decode_workspace_size(S, H, Hk, D, 0)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    P = binding._ptr
+    nc, nd = ctypes.c_int(0), ctypes.c_int(0)
+    host_s = 0.0
+
+    def step():
+        nonlocal host_s
+        t0 = time.perf_counter()
+        rc = lib.pa_bm_append_batch(bm._h, S, P(seqs), P(ones), P(slots_h), P(copies_h), ctypes.addressof(nc),
+                                    ctypes.addressof(nd))
+        rc = rc or lib.pa_bm_export(bm._h, P(tables_h), P(lens_h))
+        host_s += time.perf_counter() - t0
+        if rc:
+            raise RuntimeError(binding.pa_last_error())
+        slots_d.copy_(slots_h, non_blocking=True)
+        tables_d.copy_(tables_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        if lib.pa_write_cache(P(k_new), P(v_new), P(slots_d), P(k_cache), P(v_cache), S, Hk, D, bs, nb, sh,
+                              binding.dtype_code(tdt)):
+            raise RuntimeError(binding.pa_last_error())
+        if lib.pa_decode_ws(P(out), P(q), P(k_cache), P(v_cache), P(tables_d), P(lens_d), S, H, Hk, D, bs, mb,
+                            1 / math.sqrt(D), sh, binding.dtype_code(tdt), P(ws), ws_bytes):
+            raise RuntimeError(binding.pa_last_error())
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    tokens0 = int(sum(bm.context_len(s_) for s_ in range(S)))
+    host_s = 0.0
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    tokens1 = int(sum(bm.context_len(s_) for s_ in range(S)))
+    e = 2 if sp.dtype == "bf16" else 4
+    mean_tokens = (tokens0 + tokens1) / 2
+    kv = mean_tokens * 2 * Hk * D * e
+    line = {
+        "metric": "steady-state paged decode loop (block manager + cache write + decode), us/step",
+        "value": wall / steps * 1e6, "unit": "us/step", "higher_is_better": False, "steps": steps,
+        "warmup": args.warmup, "host_manager_us_per_step": host_s / steps * 1e6,
+        "effective_kv_gbs": kv / (wall / steps) / 1e9, "n_gpus": 1, "dtype": sp.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": S, "block_size": bs, "num_physical_blocks": nb,
+                   "context_tokens_start": tokens0, "context_tokens_end": tokens1},
+    }
+    print(json.dumps(line), flush=True)
+    bm.close()
+    return 0
+
+
+def dataclasses_replace(sp, **kw):
+    import dataclasses
+
+    return dataclasses.replace(sp, **kw)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -470,11 +575,15 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the step captured in a CUDA graph (region 1) instead of eager calls")
     ap.add_argument("--block-size", type=int, default=None, help="override the workload's block size")
+    ap.add_argument("--loop", action="store_true",
+                    help="steady-state decode loop driven by the host block manager (separate metric)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.loop:
+        return run_loop(args)
     return run_ours(args)
 
 

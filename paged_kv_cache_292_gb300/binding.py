@@ -31,7 +31,9 @@ PA_DEVERR_CONTEXT_LEN = 2
 PA_DEVERR_SLOT = 4
 PA_DEVERR_TIMEOUT = 8
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pagedattn.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "pagedattn.h")
+PA_ERR_NO_BLOCKS = -5
 
 
 class PagedAttnError(RuntimeError):
@@ -56,6 +58,18 @@ _SIGS = {
     "pa_write_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I]),
     "pa_write_cache_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P]),
     "pa_last_error": (ctypes.c_char_p, []),
+    "pa_bm_create": (_P, [_I, _I, _I, _I]),
+    "pa_bm_destroy": (None, [_P]),
+    "pa_bm_num_free_blocks": (_I, [_P]),
+    "pa_bm_context_len": (_I, [_P, _I]),
+    "pa_bm_ref_count": (_I, [_P, _I]),
+    "pa_bm_append": (_I, [_P, _I, _I, _P, _P, _P]),
+    "pa_bm_fork": (_I, [_P, _I, _I]),
+    "pa_bm_append_batch": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
+    "pa_bm_share_prefix": (_I, [_P, _I, _I, _I]),
+    "pa_bm_free": (_I, [_P, _I]),
+    "pa_bm_export": (_I, [_P, _P, _P]),
+    "pa_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _I]),
     "pa_version": (_I, []),
 }
 
@@ -80,11 +94,15 @@ def load() -> ctypes.CDLL:
 
 
 def header_symbols() -> list:
-    """Names of the functions the public header declares."""
-    with open(HEADER) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", text)))
+    """Names of the functions the public headers (include/*.h) declare."""
+    names = set()
+    for fn in sorted(os.listdir(INCLUDE)):
+        if not fn.endswith(".h"):
+            continue
+        with open(os.path.join(INCLUDE, fn)) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        names |= set(re.findall(r"\b(pa_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def _ptr(x) -> Optional[int]:
@@ -218,3 +236,81 @@ def write_cache(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None, *, er
     NB, bs = k_cache.shape[:2]
     pa_write_cache_ex(k_new, v_new, slot_mapping, k_cache, v_cache, T, Hk, D, bs, NB, stream,
                       dtype_code(k_new.dtype), error_flag)
+
+
+def pa_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_kv_heads, head_size, block_size, num_physical_blocks,
+                   stream=None, dtype=None):
+    dtype = dtype_code(k_cache.dtype) if dtype is None else dtype
+    _check(load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), num_pairs, num_kv_heads, head_size,
+                                 block_size, num_physical_blocks, _stream(stream), dtype))
+
+
+class BlockManager:
+    """The C block manager (pa_bm_*): host memory only, no device calls."""
+
+    def __init__(self, num_blocks, block_size, max_seqs, max_blocks_per_seq):
+        lib = load()
+        self._h = lib.pa_bm_create(num_blocks, block_size, max_seqs, max_blocks_per_seq)
+        if not self._h:
+            raise PagedAttnError(PA_ERR_INVALID_ARG, pa_last_error())
+        self.num_blocks, self.block_size = num_blocks, block_size
+        self.max_seqs, self.max_blocks_per_seq = max_seqs, max_blocks_per_seq
+
+    def close(self):
+        if self._h:
+            load().pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free_blocks(self):
+        return load().pa_bm_num_free_blocks(self._h)
+
+    def context_len(self, seq):
+        return load().pa_bm_context_len(self._h, seq)
+
+    def ref_count(self, block):
+        return load().pa_bm_ref_count(self._h, block)
+
+    def append(self, seq, num_tokens):
+        """Slots (int64 tensor) for num_tokens new tokens, and the list of (src, dst) block copies."""
+        slots = torch.empty(max(num_tokens, 1), dtype=torch.int64)
+        copies = (ctypes.c_int32 * 2)()
+        n = ctypes.c_int(0)
+        _check(load().pa_bm_append(self._h, seq, num_tokens, slots.data_ptr(), ctypes.addressof(copies),
+                                   ctypes.addressof(n)))
+        return slots[:num_tokens], [(copies[0], copies[1])] if n.value else []
+
+    def append_batch(self, seqs, counts, slots_out=None, copies_out=None):
+        """One call for many sequences; returns (slots, list of (src, dst) copies)."""
+        seqs = torch.as_tensor(seqs, dtype=torch.int32)
+        counts = torch.as_tensor(counts, dtype=torch.int32)
+        total = int(counts.sum())
+        if slots_out is None:
+            slots_out = torch.empty(max(total, 1), dtype=torch.int64)
+        if copies_out is None:
+            copies_out = torch.empty(2 * max(len(seqs), 1), dtype=torch.int32)
+        nc, nd = ctypes.c_int(0), ctypes.c_int(0)
+        _check(load().pa_bm_append_batch(self._h, len(seqs), seqs.data_ptr(), counts.data_ptr(), slots_out.data_ptr(),
+                                         copies_out.data_ptr(), ctypes.addressof(nc), ctypes.addressof(nd)))
+        pairs = copies_out[: 2 * nc.value].view(-1, 2)
+        return slots_out[:total], [tuple(p) for p in pairs.tolist()]
+
+    def fork(self, parent, child):
+        _check(load().pa_bm_fork(self._h, parent, child))
+
+    def share_prefix(self, seq, donor, num_tokens):
+        _check(load().pa_bm_share_prefix(self._h, seq, donor, num_tokens))
+
+    def free(self, seq):
+        _check(load().pa_bm_free(self._h, seq))
+
+    def export(self):
+        tables = torch.empty((self.max_seqs, self.max_blocks_per_seq), dtype=torch.int32)
+        lens = torch.empty(self.max_seqs, dtype=torch.int32)
+        _check(load().pa_bm_export(self._h, tables.data_ptr(), lens.data_ptr()))
+        return tables, lens

@@ -106,3 +106,51 @@ extern "C" int pa_write_cache_ex(const void* k_new, const void* v_new,
                               num_kv_heads, head_size, block_size, num_physical_blocks, stream,
                               dtype, error_flag);
 }
+
+// ---------------------------------------------------------------------------
+// Copy-on-write support: whole-block copies inside both pools.
+// ---------------------------------------------------------------------------
+namespace pa {
+
+__global__ void __launch_bounds__(256) pa_copy_blocks_kernel(uint4* __restrict__ k_cache,
+                                                             uint4* __restrict__ v_cache,
+                                                             const int32_t* __restrict__ pairs,
+                                                             int num_pairs, int block_vecs,
+                                                             int num_blocks) {
+  griddep_wait();
+  for (int i = blockIdx.x; i < num_pairs; i += gridDim.x) {
+    const int src = pairs[2 * i], dst = pairs[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) continue;
+    const size_t so = (size_t)src * block_vecs, d = (size_t)dst * block_vecs;
+    for (int j = threadIdx.x; j < block_vecs; j += blockDim.x) {
+      k_cache[d + j] = k_cache[so + j];
+      v_cache[d + j] = v_cache[so + j];
+    }
+  }
+}
+
+}  // namespace pa
+
+extern "C" int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                              int num_kv_heads, int head_size, int block_size,
+                              int num_physical_blocks, void* stream, int dtype) {
+  pa::clear_error();
+  if (!k_cache || !v_cache || (num_pairs > 0 && !pairs))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: null pointer");
+  if (num_pairs < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_physical_blocks <= 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: sizes must be positive");
+  if (dtype != PA_F32 && dtype != PA_BF16) return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: dtype %d", dtype);
+  const long long bytes = (long long)block_size * num_kv_heads * head_size * (dtype == PA_F32 ? 4 : 2);
+  if (bytes % 16 != 0 || bytes / 16 > (1ll << 30))
+    return pa::fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: block of %lld bytes", bytes);
+  if (!pa::aligned(k_cache, 16) || !pa::aligned(v_cache, 16) || !pa::aligned(pairs, 4))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: misaligned pointer");
+  if (num_pairs == 0) return PA_OK;
+  const int grid = num_pairs < 65535 ? num_pairs : 65535;
+  pa::pa_copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), pairs, num_pairs,
+      static_cast<int>(bytes / 16), num_physical_blocks);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pa::cuda_fail(e, "launch pa_copy_blocks_kernel");
+  return PA_OK;
+}
