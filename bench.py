@@ -495,10 +495,15 @@ def run_loop(args):
         bm.append(s_, c - 1)  # the prompt's K/V already sits in the (random) pool
     seqs = torch.arange(S, dtype=torch.int32)
     ones = torch.ones(S, dtype=torch.int32)
-    slots_h = torch.empty(S, dtype=torch.int64).pin_memory()
+    # Two sets of pinned host buffers, each reused only after the event that
+    # follows its host-to-device copies has completed: the host never
+    # overwrites a buffer an in-flight copy still reads.
+    bufs = [dict(slots=torch.empty(S, dtype=torch.int64).pin_memory(),
+                 tables=torch.empty((S, mb), dtype=torch.int32).pin_memory(),
+                 lens=torch.empty(S, dtype=torch.int32).pin_memory(),
+                 copied=torch.cuda.Event()) for _ in range(2)]
     copies_h = torch.empty(2 * S, dtype=torch.int32)
-    tables_h = torch.empty((S, mb), dtype=torch.int32).pin_memory()
-    lens_h = torch.empty(S, dtype=torch.int32).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
     slots_d = torch.empty(S, dtype=torch.int64, device=dev)
     tables_d = torch.empty((S, mb), dtype=torch.int32, device=dev)
     lens_d = torch.empty(S, dtype=torch.int32, device=dev)
@@ -510,24 +515,29 @@ def run_loop(args):
     P = binding._ptr
     nc, nd = ctypes.c_int(0), ctypes.c_int(0)
     host_s = 0.0
+    it = 0
 
     def step():
-        nonlocal host_s
+        nonlocal host_s, it
+        b = bufs[it % 2]
+        it += 1
+        b["copied"].synchronize()  # the copy that last read these buffers is done
         t0 = time.perf_counter()
-        rc = lib.pa_bm_append_batch(bm._h, S, P(seqs), P(ones), P(slots_h), P(copies_h), ctypes.addressof(nc),
+        rc = lib.pa_bm_append_batch(bm._h, S, P(seqs), P(ones), P(b["slots"]), P(copies_h), ctypes.addressof(nc),
                                     ctypes.addressof(nd))
-        rc = rc or lib.pa_bm_export(bm._h, P(tables_h), P(lens_h))
+        rc = rc or lib.pa_bm_export(bm._h, P(b["tables"]), P(b["lens"]))
         host_s += time.perf_counter() - t0
         if rc:
             raise RuntimeError(binding.pa_last_error())
-        slots_d.copy_(slots_h, non_blocking=True)
-        tables_d.copy_(tables_h, non_blocking=True)
-        lens_d.copy_(lens_h, non_blocking=True)
+        slots_d.copy_(b["slots"], non_blocking=True)
+        tables_d.copy_(b["tables"], non_blocking=True)
+        lens_d.copy_(b["lens"], non_blocking=True)
+        b["copied"].record(stream)
         if lib.pa_write_cache(P(k_new), P(v_new), P(slots_d), P(k_cache), P(v_cache), S, Hk, D, bs, nb, sh,
                               binding.dtype_code(tdt)):
             raise RuntimeError(binding.pa_last_error())
-        if lib.pa_decode_ws(P(out), P(q), P(k_cache), P(v_cache), P(tables_d), P(lens_d), S, H, Hk, D, bs, mb,
-                            1 / math.sqrt(D), sh, binding.dtype_code(tdt), P(ws), ws_bytes):
+        if lib.pa_decode_ex(P(out), P(q), P(k_cache), P(v_cache), P(tables_d), P(lens_d), S, H, Hk, D, bs, mb,
+                            1 / math.sqrt(D), sh, binding.dtype_code(tdt), nb, P(ws), ws_bytes, 0, P(err)):
             raise RuntimeError(binding.pa_last_error())
 
     for _ in range(args.warmup):
@@ -540,6 +550,8 @@ def run_loop(args):
         step()
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device reported error bits {int(err.item())}")
     tokens1 = int(sum(bm.context_len(s_) for s_ in range(S)))
     e = 2 if sp.dtype == "bf16" else 4
     mean_tokens = (tokens0 + tokens1) / 2
