@@ -8,6 +8,7 @@ from .paged_attention import (  # noqa: F401
     attention,
     attention_weights,
     decode,
+    decode_multi,
     decode_partials,
     decode_split,
     gather_sequence,

@@ -46,6 +46,7 @@ __all__ = [
     "decode_partials",
     "merge_partials",
     "decode_split",
+    "decode_multi",
 ]
 
 
@@ -197,3 +198,35 @@ def decode_split(q, k_cache, v_cache, block_tables, context_lens, scale, block_s
         out[s] = merge_partials(m, l, o)
     return out
 
+
+
+def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, block_size):
+    """Several new query tokens per sequence over the paged cache, causal.
+
+    q : [S, Q, H, D].  The Q newest tokens of sequence s (already in the cache,
+    context_lens[s] counting them) sit at positions c - Q + i, i < Q; query i
+    attends to the gathered keys 0..c - Q + i (a causal mask over the
+    sequence).  A query whose position is negative (c < Q) has no keys and
+    gives zeros.  Returns out[S, Q, H, D] in float64.
+
+    This extends the decode step of "vLLM three-process architecture and the
+    PagedAttention kernel" section 3.2 (gather through the block table, then
+    standard attention) to the several-token steps the pages name: chunked
+    prefill and speculative-decoding verification (vLLM book preface, reader
+    questions; the is96 essay's feature list).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_cache = np.asarray(k_cache, dtype=np.float64)
+    v_cache = np.asarray(v_cache, dtype=np.float64)
+    num_seqs, num_q = q.shape[:2]
+    out = np.zeros(q.shape, dtype=np.float64)
+    for s in range(num_seqs):
+        ctx = int(context_lens[s])
+        k_s = gather_sequence(k_cache, block_tables[s], ctx, block_size)
+        v_s = gather_sequence(v_cache, block_tables[s], ctx, block_size)
+        for i in range(num_q):
+            pos = ctx - num_q + i
+            if pos < 0:
+                continue
+            out[s, i] = attention(q[s, i], k_s[: pos + 1], v_s[: pos + 1], scale)
+    return out

@@ -344,3 +344,54 @@ def test_write_then_decode_equals_prewritten_pool(name):
     out = oracle.decode(_np(pre.q), _np(pre.k_cache), _np(pre.v_cache), pre.block_tables.numpy(),
                         pre.context_lens.numpy(), pre.scale, sp.block_size)
     assert np.all(np.isfinite(out))
+
+
+# --- multi-query (causal) ------------------------------------------------
+
+
+def test_multi_query_with_one_query_is_decode():
+    rng = np.random.default_rng(20)
+    q, kc, vc, bt, ctx = _random_paged(rng)
+    a = oracle.decode(q, kc, vc, bt, ctx, 0.3, 4)
+    b = oracle.decode_multi(q[:, None], kc, vc, bt, ctx, 0.3, 4)[:, 0]
+    assert np.array_equal(a, b)
+
+
+def test_multi_query_matches_sdpa_with_bottom_right_causal_mask():
+    """Library cross-check: torch SDPA with an explicit mask that lets query i
+    (at position c - Q + i) see keys 0..c - Q + i."""
+    rng = np.random.default_rng(21)
+    S, Q, H, Hk, D, bs = 3, 4, 8, 2, 16, 4
+    ctx = np.array([4, 9, 23])
+    q4 = rng.standard_normal((S, Q, H, D))
+    _, kc, vc, bt, _ = _random_paged(rng, S=S, H=H, Hk=Hk, D=D, bs=bs, max_ctx=24, nb=20, ctx=ctx)
+    out = oracle.decode_multi(q4, kc, vc, bt, ctx, 0.25, bs)
+    flat_k, flat_v = kc.reshape(-1, Hk, D), vc.reshape(-1, Hk, D)
+    for s in range(S):
+        idx = [bt[s, t // bs] * bs + t % bs for t in range(ctx[s])]
+        ks = torch.from_numpy(flat_k[idx]).permute(1, 0, 2).repeat_interleave(H // Hk, 0)
+        vs = torch.from_numpy(flat_v[idx]).permute(1, 0, 2).repeat_interleave(H // Hk, 0)
+        qs = torch.from_numpy(q4[s]).permute(1, 0, 2)  # [H, Q, D]
+        pos = torch.arange(ctx[s] - Q, ctx[s])[:, None]
+        mask = torch.arange(ctx[s])[None, :] <= pos  # [Q, ctx]
+        ref = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, attn_mask=mask, scale=0.25)
+        np.testing.assert_allclose(out[s], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-13)
+
+
+def test_multi_query_prefix_consistency_and_short_context():
+    """Query i equals a one-query decode over the first c - Q + i + 1 tokens;
+    queries whose position is negative give zeros."""
+    rng = np.random.default_rng(22)
+    q, kc, vc, bt, _ = _random_paged(rng, S=2, max_ctx=23, ctx=[2, 17])
+    Q = 3
+    q3 = rng.standard_normal((2, Q, q.shape[1], q.shape[2]))
+    ctx = np.array([2, 17])
+    out = oracle.decode_multi(q3, kc, vc, bt, ctx, 0.4, 4)
+    assert np.all(out[0, 0] == 0)  # position -1
+    for s in range(2):
+        for i in range(Q):
+            pos = ctx[s] - Q + i
+            if pos < 0:
+                continue
+            one = oracle.decode(q3[:, i], kc, vc, bt, np.array([pos + 1] * 2), 0.4, 4)[s]
+            np.testing.assert_allclose(out[s, i], one, rtol=0, atol=1e-13)
