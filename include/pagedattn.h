@@ -135,6 +135,35 @@ int pa_decode_ex(void* out, const void* query, const void* k_cache, const void* 
                  int32_t* error_flag);
 
 /*
+ * pa_decode_mq - several query tokens per sequence over the paged cache, with
+ * a causal mask: the chunked-prefill / speculative-decoding-verification step
+ * (named by the vLLM book preface's reader questions and the is96 essay's
+ * feature list) built on the same gather as pa_decode.
+ *
+ *   out[s, i, h, :] = attention of query[s, i, h, :] over the keys/values at
+ *                     positions 0 .. context_lens[s] - num_queries + i
+ *
+ * query, out  [num_seqs, num_queries, num_heads, head_size]
+ * The num_queries newest tokens of every sequence must already be in the pool
+ * (pa_write_cache) and counted in context_lens.  A query whose position is
+ * negative (context shorter than num_queries) gets a zero row.
+ * Requires dtype PA_BF16 and (num_heads / num_kv_heads) * num_queries <= 16;
+ * num_queries == 1 is plain decode.  Other arguments as in pa_decode_ex; the
+ * scratch size comes from pa_decode_mq_workspace_size (workspace NULL: the
+ * library's own, allocated on first use).
+ */
+int pa_decode_mq(void* out, const void* query, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                 int num_queries, int num_heads, int num_kv_heads, int head_size, int block_size,
+                 int max_blocks_per_seq, float scale, void* stream, int dtype,
+                 int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                 int32_t* error_flag);
+
+/* Scratch bytes pa_decode_mq needs (0 for invalid sizes). */
+size_t pa_decode_mq_workspace_size(int num_seqs, int num_queries, int num_heads, int num_kv_heads,
+                                   int head_size, int num_ranges);
+
+/*
  * pa_write_cache - scatter one step's new K/V rows into the paged pool
  * (the "reshape_and_cache" step).  For every token i with slot_mapping[i] >= 0:
  *   k_cache[slot / block_size, slot % block_size, :, :] = k_new[i, :, :]  (bit copy)

@@ -62,7 +62,8 @@ struct StageMeta {
   int nvalid;  // valid tokens in the tile (1..16)
   int flags;   // kSegBegin | kSegEnd | (output slot + 1) << 2 | (slot of range r0) << 4
   int r0, r1;  // first and last range touching the sequence (cut sequences only)
-  int pad0, pad1;
+  int ctx;     // the sequence's context length (causal limits of several queries)
+  int pad1;
 };
 
 struct DecodeParams {
@@ -82,6 +83,7 @@ struct DecodeParams {
   int num_ranges;       // R
   int num_physical_blocks;
   int stages, q_slots;
+  int num_queries;  // query tokens per sequence (1 for plain decode)
   uint32_t row_bytes, pitch, q_bytes, stage_bytes;
   float scale_log2;  // scale * log2(e)
 };
@@ -298,6 +300,165 @@ struct MmaConsumer {
   }
 };
 
+// bf16 tensor-core consumer for several query tokens per sequence (causal).
+// The N extent of the score fragment holds (query, head) columns: column
+// n = qi * G + g for query qi < Q and group head g < G, NT tiles of 8 columns.
+// Query qi sits at position ctx - Q + qi and sees tokens up to that position.
+template <int D, int NT>
+struct MmaConsumerMQ {
+  static constexpr int KS = D / 16;
+  uint32_t qb[NT][KS][2];
+  float acc[NT][KS][4];
+  float m_a[NT], m_b[NT], l_a[NT], l_b[NT];
+
+  __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G, int Q,
+                                                int Hg, int lane) {
+    const int t2 = 2 * (lane & 3);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = nt * 8 + (lane >> 2);
+      const bool real = n < G * Q;
+      const int qi = real ? n / G : 0, g = real ? n % G : 0;
+      const __nv_bfloat16* qh =
+          reinterpret_cast<const __nv_bfloat16*>(qslot) + ((size_t)qi * Hg * G + w * G + g) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[nt][ks][0] = real ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + t2) : 0u;
+        qb[nt][ks][1] = real ? *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + t2) : 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][ks][i] = 0.f;
+      }
+      m_a[nt] = m_b[nt] = -INFINITY;
+      l_a[nt] = l_b[nt] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint32_t k_base, uint32_t v_base, uint32_t pitch,
+                                       int nvalid, int tok0, int ctx, int G, int Q,
+                                       float scale_log2, int lane) {
+    float c[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
+    const uint32_t k_lane = k_base + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 16;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      ldmatrix_x4(a, k_lane + ks * 32);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(c[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+    }
+    const int r0 = lane >> 2;
+    const int t0 = tok0 + r0, t1 = t0 + 8;
+    uint32_t pb0[NT], pb1[NT];
+    float alpha_a[NT], alpha_b[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int na = nt * 8 + 2 * (lane & 3), nb = na + 1;
+      // Last visible position of each column's query (-1: padding column).
+      const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
+      const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
+      float s0 = c[nt][0] * scale_log2, s1 = c[nt][1] * scale_log2;
+      float s2 = c[nt][2] * scale_log2, s3 = c[nt][3] * scale_log2;
+      if (r0 >= nvalid || t0 > lim_a) s0 = -INFINITY;
+      if (r0 >= nvalid || t0 > lim_b) s1 = -INFINITY;
+      if (r0 + 8 >= nvalid || t1 > lim_a) s2 = -INFINITY;
+      if (r0 + 8 >= nvalid || t1 > lim_b) s3 = -INFINITY;
+      float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, o));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, o));
+      }
+      const float mn_a = fmaxf(m_a[nt], mx_a), mn_b = fmaxf(m_b[nt], mx_b);
+      // A column may see no token of this tile (or none yet): keep -inf out of
+      // the exponent base.
+      const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
+      const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
+      alpha_a[nt] = exp2f(m_a[nt] - base_a);
+      alpha_b[nt] = exp2f(m_b[nt] - base_b);
+      m_a[nt] = mn_a;
+      m_b[nt] = mn_b;
+      const uint32_t p_top = pack_bf16x2(exp2f(s0 - base_a), exp2f(s1 - base_b));
+      const uint32_t p_bot = pack_bf16x2(exp2f(s2 - base_a), exp2f(s3 - base_b));
+      l_a[nt] = l_a[nt] * alpha_a[nt] + bf16_lo(p_top) + bf16_lo(p_bot);
+      l_b[nt] = l_b[nt] * alpha_b[nt] + bf16_hi(p_top) + bf16_hi(p_bot);
+      pb0[nt] = movmatrix_trans(p_top);
+      pb1[nt] = movmatrix_trans(p_bot);
+    }
+    const uint32_t v_lane = v_base + ((lane & 7) + (lane >> 4) * 8) * pitch + ((lane >> 3) & 1) * 16;
+    const int t2 = 2 * (lane & 3);
+    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+    if (nvalid < kTile) {
+      keep_lo = (t2 < nvalid ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid ? 0xffff0000u : 0u);
+      keep_hi = (t2 + 8 < nvalid ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, v_lane + mt * 32);
+      a[0] &= keep_lo;
+      a[1] &= keep_lo;
+      a[2] &= keep_hi;
+      a[3] &= keep_hi;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        acc[nt][mt][0] *= alpha_a[nt];
+        acc[nt][mt][1] *= alpha_b[nt];
+        acc[nt][mt][2] *= alpha_a[nt];
+        acc[nt][mt][3] *= alpha_b[nt];
+        mma_bf16_16816(acc[nt][mt], a, pb0[nt], pb1[nt]);
+      }
+    }
+  }
+
+  // Output rows are [seq][query][head]; partial rows are [query][head].
+  __device__ __forceinline__ void finish(const DecodeParams& p, int seq, int kv_head, int slot,
+                                         int r, int lane) {
+    const int G = p.group, H = p.num_heads, Q = p.num_queries;
+    const int d0 = lane >> 2;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float la = l_a[nt], lb = l_b[nt];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        la += __shfl_xor_sync(0xffffffffu, la, o);
+        lb += __shfl_xor_sync(0xffffffffu, lb, o);
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int n = nt * 8 + 2 * (lane & 3) + half;
+        if (n >= G * Q) continue;
+        const int qi = n / G, g = n % G;
+        const int row = qi * H + kv_head * G + g;
+        const float l = half ? lb : la, m = half ? m_b[nt] : m_a[nt];
+        if (slot < 0) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)seq * Q * H + row) * D;
+          const float inv = l > 0.f ? 1.f / l : 0.f;  // a query with no keys gives zeros
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            out[mt * 16 + d0] = __float2bfloat16_rn(acc[nt][mt][half] * inv);
+            out[mt * 16 + d0 + 8] = __float2bfloat16_rn(acc[nt][mt][2 + half] * inv);
+          }
+        } else {
+          const size_t base = ((size_t)r * 2 + slot) * Q * H + row;
+          float* po = p.part_o + base * D;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            po[mt * 16 + d0] = acc[nt][mt][half];
+            po[mt * 16 + d0 + 8] = acc[nt][mt][2 + half];
+          }
+          if (d0 == 0) {
+            p.part_ml[base * 2 + 0] = m;
+            p.part_ml[base * 2 + 1] = l;
+          }
+        }
+      }
+    }
+  }
+};
+
 // fp32 CUDA-core consumer.  Lane l owns head dims [l*DC, l*DC+DC) of every
 // query head; after the butterfly reduction lane l holds the score of token l/2.
 template <int D, int GMAX>
@@ -442,7 +603,7 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 // (seq, kv_head).  Takes a ticket; the warp holding the last of the r1-r0+1
 // tickets merges every partial of that sequence and KV head by log-sum-exp,
 // writes the output rows, and resets the ticket counter.  Nobody waits.
-template <typename T, int D>
+template <typename T, int D, bool kMQ>
 __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, int r0, int r1,
                                  int slot0, int lane) {
   __threadfence();  // this warp's partial is visible before its ticket is
@@ -458,10 +619,14 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
   // loads are issued before the current one is folded in.
   constexpr int DL = D / 32;
   constexpr int GM = 4;
-  const int G = p.group, H = p.num_heads;
-  for (int g0 = 0; g0 < G; g0 += GM) {
-    const int h0 = kv_head * G + g0;
-    const int gn = min(GM, G - g0);
+  const int G = p.group, H = kMQ ? p.num_queries * p.num_heads : p.num_heads;
+  const int nq = kMQ ? p.num_queries : 1;
+  for (int gq = 0, gn = 0; gq < G * nq; gq += gn) {
+    // Rows of this KV head, at most four at a time and never across queries:
+    // query qi, group heads g0 .. g0 + gn - 1.
+    const int qi = gq / G, g0 = gq % G;
+    const int h0 = qi * p.num_heads + kv_head * G + g0;
+    gn = min(GM, G - g0);
     float run_m[GM], run_l[GM], acc[GM][DL];
     float nm[GM], nl[GM], no[GM][DL];
 #pragma unroll
@@ -506,7 +671,10 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
       for (int g = 0; g < GM; ++g) {
         if (g < gn) {
           const float mnew = fmaxf(run_m[g], cm[g]);
-          const float a_old = exp2f(run_m[g] - mnew), a_new = exp2f(cm[g] - mnew);
+          // Several queries: a query may have no keys in some (or all)
+          // partials, m = -inf; keep -inf out of the exponent base.
+          const float mb = (kMQ && mnew == -INFINITY) ? 0.f : mnew;
+          const float a_old = exp2f(run_m[g] - mb), a_new = exp2f(cm[g] - mb);
           run_m[g] = mnew;
           run_l[g] = run_l[g] * a_old + cl[g] * a_new;
 #pragma unroll
@@ -518,7 +686,7 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
       if (g < gn) {
-        const float inv = 1.f / run_l[g];
+        const float inv = (kMQ && run_l[g] == 0.f) ? 0.f : 1.f / run_l[g];
 #pragma unroll
         for (int i = 0; i < DL; ++i) out[(size_t)g * D + i] = T(acc[g][i] * inv);
       }
@@ -531,7 +699,9 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 // ---------------------------------------------------------------------------
 // Kernel 1
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX>
+// QMODE 0: one query per sequence.  QMODE 1 / 2: several query tokens per
+// sequence with a causal mask, (query, head) columns in one / two MMA N-tiles.
+template <typename T, int D, int GMAX, int QMODE>
 __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     pa_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -676,8 +846,17 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         if (lane == 0) {
           const uint32_t qb = qfull_bar(qi);
           mbar_arrive_expect_tx(qb, p.q_bytes);
-          bulk_copy_g2s(qring + qi * q_slot_bytes, qg + ((size_t)s * H + (size_t)hg * Hg * G) * D,
-                        p.q_bytes, qb);
+          if constexpr (QMODE == 0) {
+            bulk_copy_g2s(qring + qi * q_slot_bytes, qg + ((size_t)s * H + (size_t)hg * Hg * G) * D,
+                          p.q_bytes, qb);
+          } else {
+            // Query rows are [seq][query][head]: one copy per query token.
+            const uint32_t per_q = p.q_bytes / p.num_queries;
+            for (int qq = 0; qq < p.num_queries; ++qq)
+              bulk_copy_g2s(qring + qi * q_slot_bytes + qq * per_q,
+                            qg + (((size_t)s * p.num_queries + qq) * H + (size_t)hg * Hg * G) * D,
+                            per_q, qb);
+          }
         }
         if (++qi == NQ) {
           qi = 0;
@@ -702,7 +881,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         break;
       }
       if (lane == 0) {
-        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, 0, 0};
+        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, c, 0};
         mbar_arrive_expect_tx(full_bar(st), __popc(copies) * p.row_bytes);
       }
       __syncwarp();
@@ -724,7 +903,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     int st = 0, qi = 0;
     uint32_t ph = 0, qph = 0;
     constexpr bool kMma = (sizeof(T) == 2);
-    typename std::conditional<kMma, MmaConsumer<D>, SimtConsumer<D, GMAX>>::type cons;
+    using Mma = typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, (QMODE > 0 ? QMODE : 1)>>::type;
+    typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
     for (long long x = a; x < b; ++x) {
       if (!mbar_wait(full_bar(st), ph)) {
         report(p.error_flag, PA_DEVERR_TIMEOUT);
@@ -736,7 +916,10 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
           report(p.error_flag, PA_DEVERR_TIMEOUT);
           break;
         }
-        cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, lane);
+        if constexpr (QMODE == 0)
+          cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, lane);
+        else
+          cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, p.num_queries, Hg, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty_bar(qi));
         if (++qi == NQ) {
@@ -746,7 +929,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       }
       const uint32_t k_base = stages + st * p.stage_bytes + w * D * (uint32_t)sizeof(T);
       const uint32_t v_base = k_base + kTile * p.pitch;
-      if constexpr (kMma) {
+      if constexpr (kMma && QMODE > 0) {
+        cons.tile(k_base, v_base, p.pitch, mt.nvalid, mt.tok0, mt.ctx, G, p.num_queries, p.scale_log2, lane);
+      } else if constexpr (kMma) {
         cons.tile(k_base, v_base, p.pitch, mt.nvalid, p.scale_log2, lane);
       } else {
         const unsigned char* kb = smem + L.stage + st * p.stage_bytes + w * D * sizeof(T);
@@ -757,7 +942,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       if (mt.flags & kSegEnd) {
         const int slot = ((mt.flags >> 2) & 3) - 1;
         cons.finish(p, mt.seq, kv_head, slot, r, lane);
-        if (slot >= 0) arrive_and_merge<T, D>(p, mt.seq, kv_head, mt.r0, mt.r1, (mt.flags >> 4) & 1, lane);
+        if (slot >= 0)
+          arrive_and_merge<T, D, (QMODE > 0)>(p, mt.seq, kv_head, mt.r0, mt.r1, (mt.flags >> 4) & 1, lane);
       }
       if (++st == NS) {
         st = 0;
@@ -785,7 +971,8 @@ struct Plan {
 // its last bytes (rounded down to 256), so that buffers reused across batch
 // shapes keep tickets and partials apart.
 size_t workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_size, int R,
-                        Plan* pl) {
+                        Plan* pl, int num_queries = 1) {
+  num_heads *= num_queries;  // partial rows are (query, head) pairs
   const size_t ml = align_up(sizeof(float) * (size_t)R * 2 * num_heads * 2, 256);
   const size_t o = align_up(sizeof(float) * (size_t)R * 2 * num_heads * head_size, 256);
   const size_t cnt = align_up(sizeof(int32_t) * (size_t)num_seqs * num_kv_heads, 256);
@@ -814,14 +1001,14 @@ int default_ranges(const DeviceInfo& dev, int HG) {
 }
 
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int elt,
-              int num_ranges, const DeviceInfo& dev, Plan* pl) {
+              int num_ranges, const DeviceInfo& dev, Plan* pl, int num_queries = 1) {
   const int G = num_heads / num_kv_heads;
   pl->Hg = heads_per_cta(num_kv_heads, head_size, elt);
   pl->HG = num_kv_heads / pl->Hg;
   pl->R = num_ranges > 0 ? num_ranges : default_ranges(dev, pl->HG);
   pl->row_bytes = (uint32_t)(pl->Hg * head_size * elt);
   pl->pitch = pl->row_bytes + kRowSkew;
-  pl->q_bytes = (uint32_t)(pl->Hg * G * head_size * elt);
+  pl->q_bytes = (uint32_t)(num_queries * pl->Hg * G * head_size * elt);
   pl->stage_bytes = 2u * kTile * pl->pitch;
   pl->stages = 0;
   const int pref[][2] = {{6, 2}, {5, 2}, {4, 2}, {3, 2}, {3, 1}, {2, 2}, {2, 1}};
@@ -837,7 +1024,7 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int 
   if (pl->stages == 0)
     return fail(PA_ERR_UNSUPPORTED, "decode stages (%u bytes each) do not fit in %d bytes of shared memory",
                 pl->stage_bytes, dev.max_smem_optin);
-  workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, pl->R, pl);
+  workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, pl->R, pl, num_queries);
   return PA_OK;
 }
 
@@ -893,10 +1080,10 @@ cudaError_t launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
-template <typename T, int D, int GMAX>
+template <typename T, int D, int GMAX, int QMODE = 0>
 int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream) {
   static bool configured[64] = {false};
-  auto kern = pa_decode_kernel<T, D, GMAX>;
+  auto kern = pa_decode_kernel<T, D, GMAX, QMODE>;
   if (!configured[dev]) {
     DeviceInfo info{};
     int rc = current_device_info(&info);
@@ -914,6 +1101,9 @@ int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
 template <typename T, int D>
 int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream) {
   if constexpr (sizeof(T) == 2) {
+    if (prm.num_queries > 1)  // (query, head) columns in one or two 8-wide MMA tiles
+      return prm.group * prm.num_queries <= 8 ? launch_typed<T, D, 8, 1>(prm, pl, dev, stream)
+                                               : launch_typed<T, D, 8, 2>(prm, pl, dev, stream);
     return launch_typed<T, D, 8>(prm, pl, dev, stream);  // the MMA consumer pads G to 8
   } else {
     const int G = prm.group;
@@ -926,23 +1116,29 @@ int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
 
 }  // namespace
 
-int decode_impl(void* out, const void* query, const void* k_cache, const void* v_cache,
-                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
-                int num_heads, int num_kv_heads, int head_size, int block_size,
-                int max_blocks_per_seq, float scale, void* stream, int dtype,
-                int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
-                int32_t* error_flag) {
+int decode_impl_q(void* out, const void* query, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                  int num_queries, int num_heads, int num_kv_heads, int head_size, int block_size,
+                  int max_blocks_per_seq, float scale, void* stream, int dtype,
+                  int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                  int32_t* error_flag) {
   clear_error();
   int rc = validate(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
                     num_kv_heads, head_size, block_size, max_blocks_per_seq, scale, dtype,
                     num_physical_blocks, num_ranges);
   if (rc != PA_OK) return rc;
+  if (num_queries < 1) return fail(PA_ERR_INVALID_ARG, "pa_decode_mq: num_queries %d < 1", num_queries);
+  if (num_queries > 1 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_mq: several queries need bf16");
+  if (num_queries > 1 && (num_heads / num_kv_heads) * num_queries > 16)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_mq: group size x queries = %d > 16",
+                (num_heads / num_kv_heads) * num_queries);
   DeviceInfo dev{};
   rc = current_device_info(&dev);
   if (rc != PA_OK) return rc;
   const int elt = dtype == PA_F32 ? 4 : 2;
   Plan pl{};
-  rc = make_plan(num_seqs, num_heads, num_kv_heads, head_size, elt, num_ranges, dev, &pl);
+  rc = make_plan(num_seqs, num_heads, num_kv_heads, head_size, elt, num_ranges, dev, &pl, num_queries);
   if (rc != PA_OK) return rc;
   int32_t* counters = nullptr;
   if (workspace == nullptr) {
@@ -982,6 +1178,7 @@ int decode_impl(void* out, const void* query, const void* k_cache, const void* v
   prm.num_ranges = pl.R;
   prm.num_physical_blocks = num_physical_blocks;
   prm.stages = pl.stages;
+  prm.num_queries = num_queries;
   prm.q_slots = pl.q_slots;
   prm.row_bytes = pl.row_bytes;
   prm.pitch = pl.pitch;
@@ -997,8 +1194,21 @@ int decode_impl(void* out, const void* query, const void* k_cache, const void* v
                          : launch_dtype<float, 128>(prm, pl, dev.device, st);
 }
 
-size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
-                             int num_ranges) {
+int decode_impl(void* out, const void* query, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                int num_heads, int num_kv_heads, int head_size, int block_size,
+                int max_blocks_per_seq, float scale, void* stream, int dtype,
+                int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                int32_t* error_flag) {
+  return decode_impl_q(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, 1,
+                       num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                       stream, dtype, num_physical_blocks, workspace, workspace_bytes, num_ranges,
+                       error_flag);
+}
+
+size_t decode_workspace_size_q(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                               int num_ranges, int num_queries) {
+  if (num_queries < 1) return 0;
   if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || num_ranges < 0 ||
       num_heads % num_kv_heads != 0)
     return 0;
@@ -1010,7 +1220,12 @@ size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int 
     // larger groups leave more ranges per head group.
     R = default_ranges(dev, num_kv_heads / heads_per_cta(num_kv_heads, head_size, 2));
   }
-  return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, R, nullptr);
+  return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, R, nullptr, num_queries);
+}
+
+size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                             int num_ranges) {
+  return decode_workspace_size_q(num_seqs, num_heads, num_kv_heads, head_size, num_ranges, 1);
 }
 
 }  // namespace pa
@@ -1053,4 +1268,22 @@ extern "C" int pa_decode_ex(void* out, const void* query, const void* k_cache, c
 extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                            int head_size, int num_ranges) {
   return pa::decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, num_ranges);
+}
+
+extern "C" int pa_decode_mq(void* out, const void* query, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            int num_seqs, int num_queries, int num_heads, int num_kv_heads,
+                            int head_size, int block_size, int max_blocks_per_seq, float scale,
+                            void* stream, int dtype, int num_physical_blocks, void* workspace,
+                            size_t workspace_bytes, int num_ranges, int32_t* error_flag) {
+  return pa::decode_impl_q(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                           num_queries, num_heads, num_kv_heads, head_size, block_size,
+                           max_blocks_per_seq, scale, stream, dtype, num_physical_blocks, workspace,
+                           workspace_bytes, num_ranges, error_flag);
+}
+
+extern "C" size_t pa_decode_mq_workspace_size(int num_seqs, int num_queries, int num_heads,
+                                              int num_kv_heads, int head_size, int num_ranges) {
+  return pa::decode_workspace_size_q(num_seqs, num_heads, num_kv_heads, head_size, num_ranges,
+                                     num_queries);
 }
