@@ -209,13 +209,19 @@ struct MmaConsumer {
     const float alpha_a = exp2f(m_a - base_a), alpha_b = exp2f(m_b - base_b);
     m_a = mn_a;
     m_b = mn_b;
-    const uint32_t p_top = pack_bf16x2(exp2f(s0 - base_a), exp2f(s1 - base_b));
-    const uint32_t p_bot = pack_bf16x2(exp2f(s2 - base_a), exp2f(s3 - base_b));
-    // The sum uses the rounded weights the P.V product sees.
-    l_a = l_a * alpha_a + bf16_lo(p_top) + bf16_lo(p_bot);
-    l_b = l_b * alpha_b + bf16_hi(p_top) + bf16_hi(p_bot);
+    const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
+    const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+    // P enters the bf16 MMA as a high and a low bf16 part (P = hi + lo to
+    // about 2^-16), so the weights keep fp32-like precision.
+    const uint32_t p_top = pack_bf16x2(p0, p1), p_bot = pack_bf16x2(p2, p3);
+    const uint32_t r_top = pack_bf16x2(p0 - bf16_lo(p_top), p1 - bf16_hi(p_top));
+    const uint32_t r_bot = pack_bf16x2(p2 - bf16_lo(p_bot), p3 - bf16_hi(p_bot));
+    l_a = l_a * alpha_a + p0 + p2;
+    l_b = l_b * alpha_b + p1 + p3;
     const uint32_t pb0 = movmatrix_trans(p_top);  // P^T rows (tokens) 0-7
     const uint32_t pb1 = movmatrix_trans(p_bot);  // tokens 8-15
+    const uint32_t rb0 = movmatrix_trans(r_top);
+    const uint32_t rb1 = movmatrix_trans(r_bot);
 
     // O^T += V^T * P^T : rows = head dims, columns = query heads.
     const uint32_t v_lane = v_base + ((lane & 7) + (lane >> 4) * 8) * pitch + ((lane >> 3) & 1) * 16;
@@ -240,6 +246,7 @@ struct MmaConsumer {
       acc[mt][2] *= alpha_a;
       acc[mt][3] *= alpha_b;
       mma_bf16_16816(acc[mt], a, pb0, pb1);
+      mma_bf16_16816(acc[mt], a, rb0, rb1);
     }
   }
 
@@ -351,7 +358,7 @@ struct MmaConsumerMQ {
     }
     const int r0 = lane >> 2;
     const int t0 = tok0 + r0, t1 = t0 + 8;
-    uint32_t pb0[NT], pb1[NT];
+    uint32_t pb0[NT], pb1[NT], rb0[NT], rb1[NT];
     float alpha_a[NT], alpha_b[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -380,12 +387,17 @@ struct MmaConsumerMQ {
       alpha_b[nt] = exp2f(m_b[nt] - base_b);
       m_a[nt] = mn_a;
       m_b[nt] = mn_b;
-      const uint32_t p_top = pack_bf16x2(exp2f(s0 - base_a), exp2f(s1 - base_b));
-      const uint32_t p_bot = pack_bf16x2(exp2f(s2 - base_a), exp2f(s3 - base_b));
-      l_a[nt] = l_a[nt] * alpha_a[nt] + bf16_lo(p_top) + bf16_lo(p_bot);
-      l_b[nt] = l_b[nt] * alpha_b[nt] + bf16_hi(p_top) + bf16_hi(p_bot);
+      const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
+      const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+      const uint32_t p_top = pack_bf16x2(p0, p1), p_bot = pack_bf16x2(p2, p3);
+      const uint32_t r_top = pack_bf16x2(p0 - bf16_lo(p_top), p1 - bf16_hi(p_top));
+      const uint32_t r_bot = pack_bf16x2(p2 - bf16_lo(p_bot), p3 - bf16_hi(p_bot));
+      l_a[nt] = l_a[nt] * alpha_a[nt] + p0 + p2;
+      l_b[nt] = l_b[nt] * alpha_b[nt] + p1 + p3;
       pb0[nt] = movmatrix_trans(p_top);
       pb1[nt] = movmatrix_trans(p_bot);
+      rb0[nt] = movmatrix_trans(r_top);
+      rb1[nt] = movmatrix_trans(r_bot);
     }
     const uint32_t v_lane = v_base + ((lane & 7) + (lane >> 4) * 8) * pitch + ((lane >> 3) & 1) * 16;
     const int t2 = 2 * (lane & 3);
@@ -409,6 +421,7 @@ struct MmaConsumerMQ {
         acc[nt][mt][2] *= alpha_a[nt];
         acc[nt][mt][3] *= alpha_b[nt];
         mma_bf16_16816(acc[nt][mt], a, pb0[nt], pb1[nt]);
+        mma_bf16_16816(acc[nt][mt], a, rb0[nt], rb1[nt]);
       }
     }
   }

@@ -58,11 +58,23 @@ def oracle_decode(w, k_cache=None, v_cache=None, seqs=None):
     return oracle.decode(q, kc, vc, bt2, ctx, w.scale, bs)
 
 
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half a bf16 unit in the last place at |x| (8 significant bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0**-126)))
+    return 2.0 ** (e - 8)
+
+
 def assert_close(got: torch.Tensor, want: np.ndarray, dtype: str, what: str = ""):
     g = got.double().cpu().numpy()
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
     err = np.abs(g - want)
     max_tol, mean_tol = TOL[dtype]
+    if dtype == "bf16":
+        # The result is stored in bf16: rounding it costs up to half an ulp.
+        # Below |out| = 4 that is at most 2^-7 and fits inside 1e-2; above it
+        # the half ulp alone passes 1e-2, so only the excess over 2^-7 is
+        # allowed on top there.  Below 4 the bound stays exactly 1e-2.
+        err = np.maximum(err - np.maximum(bf16_half_ulp(want) - 2.0**-7, 0.0), 0.0)
     assert err.max() <= max_tol, f"{what}: max abs err {err.max():.3e} > {max_tol}"
     if mean_tol is not None:
         assert err.mean() <= mean_tol, f"{what}: mean abs err {err.mean():.3e} > {mean_tol}"
