@@ -298,22 +298,47 @@ def run_ours(args):
     dt = binding.dtype_code(w.q.dtype)
     g = {k: getattr(w, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_tables", "context_lens",
                                              "slot_mapping", "k_new", "v_new")}
+    Q = args.queries
+    if Q > 1:
+        # Several new tokens per sequence (positions c-Q .. c-1): their query
+        # rows, their K/V rows and their slots; the pool already holds them.
+        gen = torch.Generator().manual_seed(sp.seed + 77)
+        g["q"] = torch.randn(S, Q, H, D, generator=gen).to(w.q.dtype).to(dev)
+        g["k_new"] = torch.randn(S * Q, Hk, D, generator=gen).to(w.q.dtype).to(dev)
+        g["v_new"] = torch.randn(S * Q, Hk, D, generator=gen).to(w.q.dtype).to(dev)
+        slots = []
+        for s_, c in enumerate(w.context_lens.tolist()):
+            for i in range(Q):
+                pos = c - Q + i
+                slots.append(-1 if pos < 0 else int(w.block_tables[s_, pos // bs]) * bs + pos % bs)
+        g["slot_mapping"] = torch.tensor(slots, dtype=torch.int64, device=dev)
+        e_ = 2 if sp.dtype == "bf16" else 4
+        extra = (Q - 1) * S * (2 * H * D * e_ + 2 * 2 * Hk * D * e_ + 8)
+        by = dict(by, decode=by["decode"] + (Q - 1) * 2 * S * H * D * e_)
+        by["step"] += extra
+    n_new = S * Q
     out = torch.empty_like(g["q"])
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    ws_bytes = lib.pa_decode_workspace_size(S, H, Hk, D, 0)
+    ws_bytes = (lib.pa_decode_workspace_size(S, H, Hk, D, 0) if Q == 1
+                else lib.pa_decode_mq_workspace_size(S, Q, H, Hk, D, 0))
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # merge tickets start at zero
     P = binding._ptr
 
     def write(gg, sh=sh):
         rc = lib.pa_write_cache(P(gg["k_new"]), P(gg["v_new"]), P(gg["slot_mapping"]), P(g["k_cache"]),
-                                P(g["v_cache"]), S, Hk, D, bs, NB, sh, dt)
+                                P(g["v_cache"]), n_new, Hk, D, bs, NB, sh, dt)
         if rc:
             raise RuntimeError(binding.pa_last_error())
 
     def decode(gg, o, sh=sh):
-        rc = lib.pa_decode_ws(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
-                              P(gg["context_lens"]), S, H, Hk, D, bs, MB, w.scale, sh, dt, P(ws), ws_bytes)
+        if Q == 1:
+            rc = lib.pa_decode_ws(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
+                                  P(gg["context_lens"]), S, H, Hk, D, bs, MB, w.scale, sh, dt, P(ws), ws_bytes)
+        else:
+            rc = lib.pa_decode_mq(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
+                                  P(gg["context_lens"]), S, Q, H, Hk, D, bs, MB, w.scale, sh, dt, 0, P(ws),
+                                  ws_bytes, 0, None)
         if rc:
             raise RuntimeError(binding.pa_last_error())
 
@@ -370,7 +395,7 @@ def run_ours(args):
     value = job_throughput(by["step"], world, ms_step)
 
     # ---- end to end through the public API, host buffers ----
-    host = {k: getattr(w, k).pin_memory() for k in ("q", "block_tables", "context_lens", "slot_mapping", "k_new",
+    host = {k: g[k].cpu().pin_memory() for k in ("q", "block_tables", "context_lens", "slot_mapping", "k_new",
                                                     "v_new")}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -430,6 +455,7 @@ def run_ours(args):
             "l2": f"inputs larger than L2: {by['kv_logical'] / 1e9:.3f} GB of K/V read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
             "replicas": world,
+            "queries_per_seq": Q,
             "launch": "CUDA graph replay" if args.graph else "eager (programmatic dependent launch)",
         },
         "roofline": {
@@ -587,6 +613,8 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="time replays of the step captured in a CUDA graph (region 1) instead of eager calls")
     ap.add_argument("--block-size", type=int, default=None, help="override the workload's block size")
+    ap.add_argument("--queries", type=int, default=1,
+                    help="query tokens per sequence (several: causal multi-query step via pa_decode_mq)")
     ap.add_argument("--loop", action="store_true",
                     help="steady-state decode loop driven by the host block manager (separate metric)")
     args = ap.parse_args()
