@@ -715,7 +715,9 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 // QMODE 0: one query per sequence.  QMODE 1 / 2: several query tokens per
 // sequence with a causal mask, (query, head) columns in one / two MMA N-tiles.
 template <typename T, int D, int GMAX, int QMODE>
-__device__ __forceinline__ void decode_body(const DecodeParams& p, unsigned char* smem) {
+__global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
+    pa_decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
   const int HG = p.num_head_groups, R = p.num_ranges, S = p.num_seqs;
@@ -966,22 +968,6 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, unsigned char
   (void)Hk;
 }
 
-template <typename T, int D, int GMAX, int QMODE>
-__global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
-    pa_decode_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  decode_body<T, D, GMAX, QMODE>(p, smem);
-}
-
-// The two-tile multi-query consumer holds twice the accumulators; with nine
-// warps the launch bound above caps threads at 168 registers, so this entry
-// point states the register budget directly (9 warps x 224 fits the file).
-template <typename T, int D, int GMAX, int QMODE>
-__global__ void __maxnreg__(224) pa_decode_kernel_wide(const DecodeParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  decode_body<T, D, GMAX, QMODE>(p, smem);
-}
-
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -1110,12 +1096,7 @@ cudaError_t launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStre
 template <typename T, int D, int GMAX, int QMODE = 0>
 int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream) {
   static bool configured[64] = {false};
-  auto kern = [] {
-    if constexpr (QMODE == 2)
-      return pa_decode_kernel_wide<T, D, GMAX, QMODE>;
-    else
-      return pa_decode_kernel<T, D, GMAX, QMODE>;
-  }();
+  auto kern = pa_decode_kernel<T, D, GMAX, QMODE>;
   if (!configured[dev]) {
     DeviceInfo info{};
     int rc = current_device_info(&info);
