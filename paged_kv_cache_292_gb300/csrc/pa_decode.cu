@@ -317,16 +317,13 @@ struct MmaConsumerMQ {
   uint32_t qb[NT][KS][2];
   float acc[NT][KS][4];
   float m_a[NT], m_b[NT], l_a[NT], l_b[NT];
-  int col0 = 0;  // first (query, head) column this warp owns
 
-  // w: KV head within the CTA's group; col_base: first column of this warp.
   __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G, int Q,
-                                                int Hg, int lane, int col_base) {
-    col0 = col_base;
+                                                int Hg, int lane) {
     const int t2 = 2 * (lane & 3);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int n = col0 + nt * 8 + (lane >> 2);
+      const int n = nt * 8 + (lane >> 2);
       const bool real = n < G * Q;
       const int qi = real ? n / G : 0, g = real ? n % G : 0;
       const __nv_bfloat16* qh =
@@ -365,7 +362,7 @@ struct MmaConsumerMQ {
     float alpha_a[NT], alpha_b[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
+      const int na = nt * 8 + 2 * (lane & 3), nb = na + 1;
       // Last visible position of each column's query (-1: padding column).
       const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
       const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
@@ -444,7 +441,7 @@ struct MmaConsumerMQ {
       }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const int n = col0 + nt * 8 + 2 * (lane & 3) + half;
+        const int n = nt * 8 + 2 * (lane & 3) + half;
         if (n >= G * Q) continue;
         const int qi = n / G, g = n % G;
         const int row = qi * H + kv_head * G + g;
@@ -619,18 +616,16 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 // (seq, kv_head).  Takes a ticket; the warp holding the last of the r1-r0+1
 // tickets merges every partial of that sequence and KV head by log-sum-exp,
 // writes the output rows, and resets the ticket counter.  Nobody waits.
-// `arrivals`: warps writing partials per range and KV head (two when the
-// (query, head) columns of a KV head are split across two warps).
 template <typename T, int D, bool kMQ>
 __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, int r0, int r1,
-                                 int slot0, int lane, int arrivals = 1) {
+                                 int slot0, int lane) {
   __threadfence();  // this warp's partial is visible before its ticket is
   __syncwarp();
   int* cnt = p.counters + (size_t)seq * p.num_kv_heads + kv_head;
   int ticket = 0;
   if (lane == 0) ticket = atomicAdd(cnt, 1);
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
-  if (ticket != arrivals * (r1 - r0 + 1) - 1) return;
+  if (ticket != r1 - r0) return;
   __threadfence();  // every other partial is visible now
   // Online pass over the partials, four query heads of this KV head at a
   // time: lane l owns dims [l*DL, l*DL+DL) of each head.  The next partial's
@@ -728,9 +723,6 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const int HG = p.num_head_groups, R = p.num_ranges, S = p.num_seqs;
   const int r = blockIdx.x / HG, hg = blockIdx.x % HG;
   const int Hg = p.heads_per_cta;
-  // QMODE 2 splits each KV head's 16 (query, head) columns over two warps.
-  constexpr int kSplit = QMODE == 2 ? 2 : 1;
-  const int NCW = Hg * kSplit;  // consumer warps; warp NCW is the producer
   const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes);
   long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
   griddep_wait();  // inputs may come from the kernel just before (e.g. the cache write)
@@ -785,11 +777,11 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full_bar(i), 1);
-      mbar_init(empty_bar(i), NCW);
+      mbar_init(empty_bar(i), Hg);
     }
     for (int i = 0; i < NQ; ++i) {
       mbar_init(qfull_bar(i), 1);
-      mbar_init(qempty_bar(i), NCW);
+      mbar_init(qempty_bar(i), Hg);
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -802,7 +794,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const uint32_t stages = smem_addr(smem + L.stage);
   const int G = p.group, H = p.num_heads, Hk = p.num_kv_heads, bs = p.block_size;
 
-  if (warp == NCW) {
+  if (warp == Hg) {
     // ---------------- producer ----------------
     const T* kc = reinterpret_cast<const T*>(p.k_cache);
     const T* vc = reinterpret_cast<const T*>(p.v_cache);
@@ -919,13 +911,12 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     }
   } else {
     // ---------------- consumers ----------------
-    const int w = warp / kSplit;  // KV head within the group
-    const int col_base = (warp % kSplit) * 8;
+    const int w = warp;
     const int kv_head = hg * Hg + w;
     int st = 0, qi = 0;
     uint32_t ph = 0, qph = 0;
     constexpr bool kMma = (sizeof(T) == 2);
-    using Mma = typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, 1>>::type;
+    using Mma = typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, (QMODE > 0 ? QMODE : 1)>>::type;
     typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
     for (long long x = a; x < b; ++x) {
       if (!mbar_wait(full_bar(st), ph)) {
@@ -941,7 +932,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         if constexpr (QMODE == 0)
           cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, lane);
         else
-          cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, p.num_queries, Hg, lane, col_base);
+          cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, p.num_queries, Hg, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty_bar(qi));
         if (++qi == NQ) {
@@ -965,8 +956,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         const int slot = ((mt.flags >> 2) & 3) - 1;
         cons.finish(p, mt.seq, kv_head, slot, r, lane);
         if (slot >= 0)
-          arrive_and_merge<T, D, (QMODE > 0)>(p, mt.seq, kv_head, mt.r0, mt.r1, (mt.flags >> 4) & 1, lane,
-                                              kSplit);
+          arrive_and_merge<T, D, (QMODE > 0)>(p, mt.seq, kv_head, mt.r0, mt.r1, (mt.flags >> 4) & 1, lane);
       }
       if (++st == NS) {
         st = 0;
@@ -984,7 +974,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
 namespace {
 
 struct Plan {
-  int Hg, HG, R, stages, q_slots, split;
+  int Hg, HG, R, stages, q_slots;
   uint32_t row_bytes, pitch, q_bytes, stage_bytes, smem;
   size_t ws_ml, ws_o, ws_partials, ws_counters, ws_total;
 };
@@ -1012,8 +1002,8 @@ size_t workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_
 // KV heads one CTA stages per token row: the largest divisor of num_kv_heads
 // that is at most 8 (one consumer warp each) and keeps the row within 2 KiB,
 // so three stages fit in shared memory.
-int heads_per_cta(int num_kv_heads, int head_size, int elt, int max_heads = kMaxGroupHeads) {
-  for (int h = max_heads; h > 1; --h)
+int heads_per_cta(int num_kv_heads, int head_size, int elt) {
+  for (int h = kMaxGroupHeads; h > 1; --h)
     if (num_kv_heads % h == 0 && h * head_size * elt <= kMaxRowBytes) return h;
   return 1;
 }
@@ -1023,15 +1013,10 @@ int default_ranges(const DeviceInfo& dev, int HG) {
   return r < 1 ? 1 : r;
 }
 
-// Consumer warps per KV head: two when a KV head has more than 8 (query, head)
-// columns (one 8-wide MMA tile per warp), else one.
-int column_split(int group, int num_queries) { return group * num_queries > 8 ? 2 : 1; }
-
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int elt,
               int num_ranges, const DeviceInfo& dev, Plan* pl, int num_queries = 1) {
   const int G = num_heads / num_kv_heads;
-  pl->split = column_split(G, num_queries);
-  pl->Hg = heads_per_cta(num_kv_heads, head_size, elt, kMaxGroupHeads / pl->split);
+  pl->Hg = heads_per_cta(num_kv_heads, head_size, elt);
   pl->HG = num_kv_heads / pl->Hg;
   pl->R = num_ranges > 0 ? num_ranges : default_ranges(dev, pl->HG);
   pl->row_bytes = (uint32_t)(pl->Hg * head_size * elt);
@@ -1121,8 +1106,7 @@ int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode smem)");
     configured[dev] = true;
   }
-  cudaError_t e =
-      launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg * pl.split + 1)), pl.smem, stream, prm);
+  cudaError_t e = launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg + 1)), pl.smem, stream, prm);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_decode_kernel");
   return PA_OK;
 }
@@ -1247,8 +1231,7 @@ size_t decode_workspace_size_q(int num_seqs, int num_heads, int num_kv_heads, in
     if (current_device_info(&dev) != PA_OK) return 0;
     // The head grouping depends on the element size; size for bf16, whose
     // larger groups leave more ranges per head group.
-    const int split = column_split(num_heads / num_kv_heads, num_queries);
-    R = default_ranges(dev, num_kv_heads / heads_per_cta(num_kv_heads, head_size, 2, kMaxGroupHeads / split));
+    R = default_ranges(dev, num_kv_heads / heads_per_cta(num_kv_heads, head_size, 2));
   }
   return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, R, nullptr, num_queries);
 }
