@@ -395,3 +395,46 @@ def test_multi_query_prefix_consistency_and_short_context():
                 continue
             one = oracle.decode(q3[:, i], kc, vc, bt, np.array([pos + 1] * 2), 0.4, 4)[s]
             np.testing.assert_allclose(out[s, i], one, rtol=0, atol=1e-13)
+
+
+# --- fp8 (E4M3) quantised cache ------------------------------------------
+
+from oracle import fp8 as ofp8  # noqa: E402
+
+
+def test_e4m3_code_table_landmarks():
+    """Values fixed by the format: bias 7, 3 mantissa bits, max 448, min subnormal 2^-9."""
+    d = ofp8.e4m3_decode(np.array([0x00, 0x01, 0x07, 0x08, 0x38, 0x7E, 0x7F, 0xFE, 0x80]))
+    assert list(d[:6]) == [0.0, 2.0**-9, 7 * 2.0**-9, 2.0**-6, 1.0, 448.0]
+    assert np.isnan(d[6]) and d[7] == -448.0 and d[8] == 0.0
+
+
+def test_e4m3_round_trip_and_ties_to_even():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF, 0x80)], dtype=np.uint8)
+    assert np.array_equal(ofp8.e4m3_encode(ofp8.e4m3_decode(codes)), codes)
+    assert ofp8.e4m3_encode([-0.0, -1e-6])[0] == 0x80 and ofp8.e4m3_encode([-1e-6])[0] == 0x80
+    # 1.0625 lies halfway between 1.0 (mantissa 000) and 1.125 (001): the even one.
+    assert ofp8.e4m3_encode([1.0625])[0] == 0x38
+    assert ofp8.e4m3_encode([1.1875])[0] == 0x3A  # between 001 and 010 -> 010
+    assert ofp8.e4m3_encode([1000.0, -1e9])[0] == 0x7E and ofp8.e4m3_encode([-1e9])[0] == 0xFE
+
+
+def test_e4m3_matches_torch_in_range():
+    """Library cross-check inside the finite range (torch gives NaN beyond 448,
+    where the reading saturates instead)."""
+    rng = np.random.default_rng(30)
+    x = np.concatenate([rng.standard_normal(20000) * 4, rng.uniform(-448, 448, 2000), rng.standard_normal(2000) * 1e-3])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ofp8.e4m3_encode(x.astype(np.float32).astype(np.float64)), ref)
+
+
+def test_fp8_decode_is_decode_of_dequantised_pool():
+    rng = np.random.default_rng(31)
+    q, kc, vc, bt, ctx = _random_paged(rng)
+    kcode = ofp8.e4m3_encode(kc / 0.5)
+    vcode = ofp8.e4m3_encode(vc / 0.25)
+    out = ofp8.decode_fp8(q, kcode, vcode, bt, ctx, 0.3, 4, 0.5, 0.25)
+    ref = oracle.decode(q, ofp8.e4m3_decode(kcode) * 0.5, ofp8.e4m3_decode(vcode) * 0.25, bt, ctx, 0.3, 4)
+    assert np.array_equal(out, ref)
+    # Quantisation error stays within half an E4M3 step of the scaled values.
+    assert np.max(np.abs(ofp8.e4m3_decode(kcode) * 0.5 - kc)) <= 0.5 * 0.5 * 2.0**-3 * np.max(np.abs(kc)) * 2
