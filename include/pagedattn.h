@@ -60,6 +60,7 @@ extern "C" {
 /* Element types. */
 #define PA_F32 0
 #define PA_BF16 1
+#define PA_FP8_E4M3 2 /* pool element only: 1 sign, 4 exponent (bias 7), 3 mantissa bits; max 448 */
 
 /* Bits OR-ed into the optional device error word. */
 #define PA_DEVERR_BLOCK_ID 1    /* block id outside [0, num_physical_blocks) */
@@ -211,6 +212,32 @@ int pa_decode_static(void* out, const void* query, const void* k_cache, const vo
                      const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                      int num_heads, int num_kv_heads, int head_size, int block_size,
                      int max_blocks_per_seq, float scale, void* stream, int dtype);
+
+/*
+ * FP8 KV pool.  The pages list quantisation among vLLM's features but give no
+ * format; this library's reading: the pool holds E4M3 codes with one float
+ * scale per pool (k_scale, v_scale), a code c standing for e4m3(c) * scale.
+ *
+ * pa_write_cache_fp8 - pa_write_cache into FP8 pools: each new element x
+ * becomes the E4M3 code nearest to x / scale (the quotient in float32, ties to
+ * even, saturating at +-448).  k_new/v_new are PA_BF16 or PA_F32 (src_dtype);
+ * k_cache/v_cache are uint8 [num_physical_blocks, block_size, num_kv_heads,
+ * head_size].  error_flag as in pa_write_cache_ex (optional).
+ *
+ * pa_decode_fp8 - pa_decode_ex over FP8 pools, query and out bf16: scores use
+ * k = e4m3(code) * k_scale and values v = e4m3(code) * v_scale.  Each token
+ * moves half the bytes of a bf16 pool.  Scratch as pa_decode_workspace_size.
+ */
+int pa_write_cache_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                       void* k_cache, void* v_cache, int num_tokens, int num_kv_heads, int head_size,
+                       int block_size, int num_physical_blocks, float k_scale, float v_scale,
+                       void* stream, int src_dtype, int32_t* error_flag);
+int pa_decode_fp8(void* out, const void* query, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                  int num_heads, int num_kv_heads, int head_size, int block_size,
+                  int max_blocks_per_seq, float scale, float k_scale, float v_scale, void* stream,
+                  int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                  int32_t* error_flag);
 
 /* Message for the calling thread's last non-zero return ("" if none). */
 const char* pa_last_error(void);

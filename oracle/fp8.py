@@ -64,12 +64,19 @@ def e4m3_encode(x) -> np.ndarray:
     return np.where(np.signbit(x), mag | 0x80, mag).astype(np.uint8)
 
 
+def quantize(x, scale) -> np.ndarray:
+    """Code of x / scale.  The quotient is taken in float32 (IEEE division, as
+    the CUDA write does) and then rounded to E4M3: both sides decide each code
+    in the same precision."""
+    q = np.asarray(x, dtype=np.float32) / np.float32(scale)
+    return e4m3_encode(q.astype(np.float64))
+
+
 def write_cache_fp8(k_cache, v_cache, k_new, v_new, slot_mapping, block_size, k_scale, v_scale):
     """Quantised cache write: the scatter of paged_attention.write_cache applied
-    to e4m3_encode(k_new / k_scale) and e4m3_encode(v_new / v_scale)."""
-    kq = e4m3_encode(np.asarray(k_new, dtype=np.float64) / k_scale)
-    vq = e4m3_encode(np.asarray(v_new, dtype=np.float64) / v_scale)
-    return pa.write_cache(k_cache, v_cache, kq, vq, slot_mapping, block_size)
+    to quantize(k_new, k_scale) and quantize(v_new, v_scale)."""
+    return pa.write_cache(k_cache, v_cache, quantize(k_new, k_scale), quantize(v_new, v_scale),
+                          slot_mapping, block_size)
 
 
 def decode_fp8(q, k_codes, v_codes, block_tables, context_lens, scale, block_size, k_scale, v_scale):

@@ -26,6 +26,7 @@ PA_ERR_CUDA = -3
 PA_ERR_WORKSPACE = -4
 PA_F32 = 0
 PA_BF16 = 1
+PA_FP8_E4M3 = 2
 PA_DEVERR_BLOCK_ID = 1
 PA_DEVERR_CONTEXT_LEN = 2
 PA_DEVERR_SLOT = 4
@@ -59,6 +60,12 @@ _SIGS = {
         [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _I, _I, _P, _SZ, _I, _P],
     ),
     "pa_decode_mq_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "pa_write_cache_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, ctypes.c_float, _P, _I, _P]),
+    "pa_decode_fp8": (
+        _I,
+        [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, ctypes.c_float, ctypes.c_float, _P, _I,
+         _P, _SZ, _I, _P],
+    ),
     "pa_decode_static": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _I]),
     "pa_write_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I]),
     "pa_write_cache_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P]),
@@ -349,3 +356,30 @@ class BlockManager:
         lens = torch.empty(self.max_seqs, dtype=torch.int32)
         _check(load().pa_bm_export(self._h, tables.data_ptr(), lens.data_ptr()))
         return tables, lens
+
+
+def write_cache_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None, *,
+                    error_flag=None):
+    """Quantise and scatter k_new/v_new[T, Hk, D] (bf16 or f32) into uint8 E4M3 pools."""
+    _require_cuda(k_new, v_new, slot_mapping, k_cache, v_cache, error_flag)
+    T, Hk, D = k_new.shape
+    NB, bs = k_cache.shape[:2]
+    _check(load().pa_write_cache_fp8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), T,
+                                     Hk, D, bs, NB, float(k_scale), float(v_scale), _stream(stream),
+                                     dtype_code(k_new.dtype), _ptr(error_flag)))
+
+
+def decode_fp8(query, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale, out=None, stream=None,
+               *, num_ranges=0, workspace=None, error_flag=None, check_block_ids=False):
+    """out[S, H, D] (bf16) over uint8 E4M3 pools."""
+    _require_cuda(query, k_cache, v_cache, block_tables, context_lens, out, workspace, error_flag)
+    S, H, D = query.shape
+    NB, bs, Hk, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(query)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pa_decode_fp8(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                _ptr(context_lens), S, H, Hk, D, bs, block_tables.shape[1], float(scale),
+                                float(k_scale), float(v_scale), _stream(stream), NB if check_block_ids else 0,
+                                _ptr(workspace), ws_bytes, num_ranges, _ptr(error_flag)))
+    return out

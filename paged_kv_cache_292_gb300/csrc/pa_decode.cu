@@ -84,6 +84,7 @@ struct DecodeParams {
   int num_physical_blocks;
   int stages, q_slots;
   int num_queries;  // query tokens per sequence (1 for plain decode)
+  float v_scale;    // FP8 pools: value of a V code is decode(code) * v_scale (else 1)
   uint32_t row_bytes, pitch, q_bytes, stage_bytes;
   float scale_log2;  // scale * log2(e)
 };
@@ -472,6 +473,161 @@ struct MmaConsumerMQ {
   }
 };
 
+// Consumer for an FP8 (E4M3) pool with bf16 queries and outputs.  Codes are
+// widened to f16 in registers (exact) and both products run on f16 MMAs.
+// Q.K: as in MmaConsumer, K fragments come from 16-bit shared loads (two
+// codes of adjacent head dims).  P.V: the MMA's output rows are permuted so
+// that lane l/4 owns the adjacent dims 2*(l/4) and +1 of each 16-wide slice:
+// each A register then pairs one dim of two tokens, built from two 16-bit
+// loads with a byte permute.  Scores carry k_scale in scale_log2; v_scale is
+// applied to the finished output.
+template <int D>
+struct MmaConsumerF8 {
+  static constexpr int KS = D / 16;
+  uint32_t qb[KS][2];
+  float acc[KS][4];
+  float m_a, m_b, l_a, l_b;
+
+  __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G,
+                                                int lane) {
+    const int n = lane >> 2, t2 = 2 * (lane & 3);
+    const __nv_bfloat16* qh =
+        reinterpret_cast<const __nv_bfloat16*>(qslot) + (size_t)(w * G + n) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (n < G) {
+        const uint32_t lo = *reinterpret_cast<const uint32_t*>(qh + ks * 16 + t2);
+        const uint32_t hi = *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + t2);
+        qb[ks][0] = pack_f16x2(bf16_lo(lo), bf16_hi(lo));
+        qb[ks][1] = pack_f16x2(bf16_lo(hi), bf16_hi(hi));
+      } else {
+        qb[ks][0] = 0u;
+        qb[ks][1] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[ks][i] = 0.f;
+    }
+    m_a = m_b = -INFINITY;
+    l_a = l_b = 0.f;
+  }
+
+  __device__ __forceinline__ void tile(const unsigned char* k_base, const unsigned char* v_base,
+                                       uint32_t pitch, int nvalid, float scale_log2, int lane) {
+    const int g = lane >> 2, t2 = 2 * (lane & 3);
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    const unsigned char* k_r0 = k_base + g * pitch;
+    const unsigned char* k_r1 = k_base + (g + 8) * pitch;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      a[0] = e4m3x2_to_f16x2(*reinterpret_cast<const unsigned short*>(k_r0 + ks * 16 + t2));
+      a[1] = e4m3x2_to_f16x2(*reinterpret_cast<const unsigned short*>(k_r1 + ks * 16 + t2));
+      a[2] = e4m3x2_to_f16x2(*reinterpret_cast<const unsigned short*>(k_r0 + ks * 16 + 8 + t2));
+      a[3] = e4m3x2_to_f16x2(*reinterpret_cast<const unsigned short*>(k_r1 + ks * 16 + 8 + t2));
+      if (ks & 1)
+        mma_f16_16816(c1, a, qb[ks][0], qb[ks][1]);
+      else
+        mma_f16_16816(c0, a, qb[ks][0], qb[ks][1]);
+    }
+    float s0 = (c0[0] + c1[0]) * scale_log2, s1 = (c0[1] + c1[1]) * scale_log2;
+    float s2 = (c0[2] + c1[2]) * scale_log2, s3 = (c0[3] + c1[3]) * scale_log2;
+    if (g >= nvalid) s0 = s1 = -INFINITY;
+    if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
+    float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, o));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, o));
+    }
+    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+    const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
+    const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
+    const float alpha_a = exp2f(m_a - base_a), alpha_b = exp2f(m_b - base_b);
+    m_a = mn_a;
+    m_b = mn_b;
+    const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
+    const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+    const uint32_t p_top = pack_f16x2(p0, p1), p_bot = pack_f16x2(p2, p3);
+    const uint32_t r_top = pack_f16x2(p0 - f16_lo(p_top), p1 - f16_hi(p_top));
+    const uint32_t r_bot = pack_f16x2(p2 - f16_lo(p_bot), p3 - f16_hi(p_bot));
+    l_a = l_a * alpha_a + p0 + p2;
+    l_b = l_b * alpha_b + p1 + p3;
+    const uint32_t pb0 = movmatrix_trans(p_top), pb1 = movmatrix_trans(p_bot);
+    const uint32_t rb0 = movmatrix_trans(r_top), rb1 = movmatrix_trans(r_bot);
+    // V rows of this lane's tokens; rows past the end read as code 0 (+0.0).
+    const bool ok0 = t2 < nvalid, ok1 = t2 + 1 < nvalid, ok8 = t2 + 8 < nvalid, ok9 = t2 + 9 < nvalid;
+    const unsigned char* v0 = v_base + t2 * pitch;
+    const unsigned char* v1 = v0 + pitch;
+    const unsigned char* v8 = v_base + (t2 + 8) * pitch;
+    const unsigned char* v9 = v8 + pitch;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      const int dd = mt * 16 + 2 * g;  // this lane's dims dd, dd + 1
+      const uint32_t w0 = ok0 ? *reinterpret_cast<const unsigned short*>(v0 + dd) : 0u;
+      const uint32_t w1 = ok1 ? *reinterpret_cast<const unsigned short*>(v1 + dd) : 0u;
+      const uint32_t w8 = ok8 ? *reinterpret_cast<const unsigned short*>(v8 + dd) : 0u;
+      const uint32_t w9 = ok9 ? *reinterpret_cast<const unsigned short*>(v9 + dd) : 0u;
+      uint32_t a[4];
+      a[0] = e4m3x2_to_f16x2(__byte_perm(w0, w1, 0x0040));  // dim dd, tokens t2, t2+1
+      a[1] = e4m3x2_to_f16x2(__byte_perm(w0, w1, 0x0051));  // dim dd+1
+      a[2] = e4m3x2_to_f16x2(__byte_perm(w8, w9, 0x0040));  // dim dd, tokens t2+8, t2+9
+      a[3] = e4m3x2_to_f16x2(__byte_perm(w8, w9, 0x0051));
+      acc[mt][0] *= alpha_a;
+      acc[mt][1] *= alpha_b;
+      acc[mt][2] *= alpha_a;
+      acc[mt][3] *= alpha_b;
+      mma_f16_16816(acc[mt], a, pb0, pb1);
+      mma_f16_16816(acc[mt], a, rb0, rb1);
+    }
+  }
+
+  // Output row pairs: acc[mt][0] / [2] are dims dd / dd+1 of head hA, [1] / [3] of hB.
+  __device__ __forceinline__ void finish(const DecodeParams& p, int seq, int kv_head, int slot,
+                                         int r, int lane) {
+    float la = l_a, lb = l_b;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      la += __shfl_xor_sync(0xffffffffu, la, o);
+      lb += __shfl_xor_sync(0xffffffffu, lb, o);
+    }
+    const int G = p.group, H = p.num_heads;
+    const int ha = 2 * (lane & 3), hb = ha + 1, g = lane >> 2;
+    const int qa = kv_head * G + ha, qb_ = kv_head * G + hb;
+    if (slot < 0) {
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)seq * H * D;
+      const float ia = p.v_scale / la, ib = p.v_scale / lb;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int dd = mt * 16 + 2 * g;
+        if (ha < G)
+          *reinterpret_cast<uint32_t*>(out + (size_t)qa * D + dd) = pack_bf16x2(acc[mt][0] * ia, acc[mt][2] * ia);
+        if (hb < G)
+          *reinterpret_cast<uint32_t*>(out + (size_t)qb_ * D + dd) = pack_bf16x2(acc[mt][1] * ib, acc[mt][3] * ib);
+      }
+    } else {
+      const size_t base = ((size_t)r * 2 + slot) * H;
+      float* po = p.part_o + base * D;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int dd = mt * 16 + 2 * g;
+        if (ha < G) *reinterpret_cast<float2*>(po + (size_t)qa * D + dd) = make_float2(acc[mt][0], acc[mt][2]);
+        if (hb < G) *reinterpret_cast<float2*>(po + (size_t)qb_ * D + dd) = make_float2(acc[mt][1], acc[mt][3]);
+      }
+      if (g == 0) {
+        float* pm = p.part_ml + base * 2;
+        if (ha < G) {
+          pm[(size_t)qa * 2 + 0] = m_a;
+          pm[(size_t)qa * 2 + 1] = la;
+        }
+        if (hb < G) {
+          pm[(size_t)qb_ * 2 + 0] = m_b;
+          pm[(size_t)qb_ * 2 + 1] = lb;
+        }
+      }
+    }
+  }
+};
+
 // fp32 CUDA-core consumer.  Lane l owns head dims [l*DC, l*DC+DC) of every
 // query head; after the butterfly reduction lane l holds the score of token l/2.
 template <int D, int GMAX>
@@ -699,7 +855,7 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
       if (g < gn) {
-        const float inv = (kMQ && run_l[g] == 0.f) ? 0.f : 1.f / run_l[g];
+        const float inv = (kMQ && run_l[g] == 0.f) ? 0.f : p.v_scale / run_l[g];
 #pragma unroll
         for (int i = 0; i < DL; ++i) out[(size_t)g * D + i] = T(acc[g][i] * inv);
       }
@@ -714,7 +870,7 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 // ---------------------------------------------------------------------------
 // QMODE 0: one query per sequence.  QMODE 1 / 2: several query tokens per
 // sequence with a causal mask, (query, head) columns in one / two MMA N-tiles.
-template <typename T, int D, int GMAX, int QMODE>
+template <typename T, int D, int GMAX, int QMODE, bool KV8 = false>
 __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     pa_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -796,8 +952,10 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
 
   if (warp == Hg) {
     // ---------------- producer ----------------
-    const T* kc = reinterpret_cast<const T*>(p.k_cache);
-    const T* vc = reinterpret_cast<const T*>(p.v_cache);
+    // Pool element: T, or one byte for an FP8 pool.
+    using KV = typename std::conditional<KV8, unsigned char, T>::type;
+    const KV* kc = reinterpret_cast<const KV*>(p.k_cache);
+    const KV* vc = reinterpret_cast<const KV*>(p.v_cache);
     const T* qg = reinterpret_cast<const T*>(p.q);
     int s = s_first;
     long long ps = p_first;
@@ -900,7 +1058,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       __syncwarp();
       if (ok) {
         const size_t row = ((size_t)phys * bs + tok % bs) * Hk + (size_t)hg * Hg;
-        const T* src = (is_v ? vc : kc) + row * D;
+        const KV* src = (is_v ? vc : kc) + row * D;
         const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
         bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
       }
@@ -916,7 +1074,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     int st = 0, qi = 0;
     uint32_t ph = 0, qph = 0;
     constexpr bool kMma = (sizeof(T) == 2);
-    using Mma = typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, (QMODE > 0 ? QMODE : 1)>>::type;
+    using Mma = typename std::conditional<
+        KV8, MmaConsumerF8<D>,
+        typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, (QMODE > 0 ? QMODE : 1)>>::type>::type;
     typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
     for (long long x = a; x < b; ++x) {
       if (!mbar_wait(full_bar(st), ph)) {
@@ -929,7 +1089,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
           report(p.error_flag, PA_DEVERR_TIMEOUT);
           break;
         }
-        if constexpr (QMODE == 0)
+        if constexpr (QMODE == 0 || KV8)
           cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, lane);
         else
           cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, p.num_queries, Hg, lane);
@@ -940,9 +1100,13 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
           qph ^= 1u;
         }
       }
-      const uint32_t k_base = stages + st * p.stage_bytes + w * D * (uint32_t)sizeof(T);
+      constexpr uint32_t kKVBytes = KV8 ? 1u : (uint32_t)sizeof(T);
+      const uint32_t k_base = stages + st * p.stage_bytes + w * D * kKVBytes;
       const uint32_t v_base = k_base + kTile * p.pitch;
-      if constexpr (kMma && QMODE > 0) {
+      if constexpr (KV8) {
+        const unsigned char* kb = smem + L.stage + st * p.stage_bytes + w * D;
+        cons.tile(kb, kb + kTile * p.pitch, p.pitch, mt.nvalid, p.scale_log2, lane);
+      } else if constexpr (kMma && QMODE > 0) {
         cons.tile(k_base, v_base, p.pitch, mt.nvalid, mt.tok0, mt.ctx, G, p.num_queries, p.scale_log2, lane);
       } else if constexpr (kMma) {
         cons.tile(k_base, v_base, p.pitch, mt.nvalid, p.scale_log2, lane);
@@ -1014,14 +1178,16 @@ int default_ranges(const DeviceInfo& dev, int HG) {
 }
 
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int elt,
-              int num_ranges, const DeviceInfo& dev, Plan* pl, int num_queries = 1) {
+              int num_ranges, const DeviceInfo& dev, Plan* pl, int num_queries = 1,
+              int q_elt = 0) {
+  if (q_elt == 0) q_elt = elt;  // query element size (differs from the pool's for FP8 pools)
   const int G = num_heads / num_kv_heads;
   pl->Hg = heads_per_cta(num_kv_heads, head_size, elt);
   pl->HG = num_kv_heads / pl->Hg;
   pl->R = num_ranges > 0 ? num_ranges : default_ranges(dev, pl->HG);
   pl->row_bytes = (uint32_t)(pl->Hg * head_size * elt);
   pl->pitch = pl->row_bytes + kRowSkew;
-  pl->q_bytes = (uint32_t)(num_queries * pl->Hg * G * head_size * elt);
+  pl->q_bytes = (uint32_t)(num_queries * pl->Hg * G * head_size * q_elt);
   pl->stage_bytes = 2u * kTile * pl->pitch;
   pl->stages = 0;
   const int pref[][2] = {{6, 2}, {5, 2}, {4, 2}, {3, 2}, {3, 1}, {2, 2}, {2, 1}};
@@ -1093,10 +1259,10 @@ cudaError_t launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
-template <typename T, int D, int GMAX, int QMODE = 0>
+template <typename T, int D, int GMAX, int QMODE = 0, bool KV8 = false>
 int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream) {
   static bool configured[64] = {false};
-  auto kern = pa_decode_kernel<T, D, GMAX, QMODE>;
+  auto kern = pa_decode_kernel<T, D, GMAX, QMODE, KV8>;
   if (!configured[dev]) {
     DeviceInfo info{};
     int rc = current_device_info(&info);
@@ -1112,8 +1278,10 @@ int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
 }
 
 template <typename T, int D>
-int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream) {
+int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream,
+                 bool kv_fp8 = false) {
   if constexpr (sizeof(T) == 2) {
+    if (kv_fp8) return launch_typed<T, D, 8, 0, true>(prm, pl, dev, stream);
     if (prm.num_queries > 1)  // (query, head) columns in one or two 8-wide MMA tiles
       return prm.group * prm.num_queries <= 8 ? launch_typed<T, D, 8, 1>(prm, pl, dev, stream)
                                                : launch_typed<T, D, 8, 2>(prm, pl, dev, stream);
@@ -1134,8 +1302,15 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
                   int num_queries, int num_heads, int num_kv_heads, int head_size, int block_size,
                   int max_blocks_per_seq, float scale, void* stream, int dtype,
                   int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
-                  int32_t* error_flag) {
+                  int32_t* error_flag, bool kv_fp8 = false, float k_scale = 1.f,
+                  float v_scale = 1.f) {
   clear_error();
+  if (kv_fp8) {
+    if (dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: query/out must be bf16");
+    if (num_queries != 1) return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: one query per sequence");
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale <= 0.f || v_scale <= 0.f)
+      return fail(PA_ERR_INVALID_ARG, "pa_decode_fp8: scales must be finite and positive");
+  }
   int rc = validate(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
                     num_kv_heads, head_size, block_size, max_blocks_per_seq, scale, dtype,
                     num_physical_blocks, num_ranges);
@@ -1151,7 +1326,8 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   if (rc != PA_OK) return rc;
   const int elt = dtype == PA_F32 ? 4 : 2;
   Plan pl{};
-  rc = make_plan(num_seqs, num_heads, num_kv_heads, head_size, elt, num_ranges, dev, &pl, num_queries);
+  rc = make_plan(num_seqs, num_heads, num_kv_heads, head_size, kv_fp8 ? 1 : elt, num_ranges, dev, &pl,
+                 num_queries, elt);
   if (rc != PA_OK) return rc;
   int32_t* counters = nullptr;
   if (workspace == nullptr) {
@@ -1197,11 +1373,12 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   prm.pitch = pl.pitch;
   prm.q_bytes = pl.q_bytes;
   prm.stage_bytes = pl.stage_bytes;
-  prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  prm.scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
+  prm.v_scale = v_scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == PA_BF16) {
-    return head_size == 64 ? launch_dtype<__nv_bfloat16, 64>(prm, pl, dev.device, st)
-                           : launch_dtype<__nv_bfloat16, 128>(prm, pl, dev.device, st);
+    return head_size == 64 ? launch_dtype<__nv_bfloat16, 64>(prm, pl, dev.device, st, kv_fp8)
+                           : launch_dtype<__nv_bfloat16, 128>(prm, pl, dev.device, st, kv_fp8);
   }
   return head_size == 64 ? launch_dtype<float, 64>(prm, pl, dev.device, st)
                          : launch_dtype<float, 128>(prm, pl, dev.device, st);
@@ -1299,4 +1476,16 @@ extern "C" size_t pa_decode_mq_workspace_size(int num_seqs, int num_queries, int
                                               int num_kv_heads, int head_size, int num_ranges) {
   return pa::decode_workspace_size_q(num_seqs, num_heads, num_kv_heads, head_size, num_ranges,
                                      num_queries);
+}
+
+extern "C" int pa_decode_fp8(void* out, const void* query, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                             int block_size, int max_blocks_per_seq, float scale, float k_scale,
+                             float v_scale, void* stream, int num_physical_blocks, void* workspace,
+                             size_t workspace_bytes, int num_ranges, int32_t* error_flag) {
+  return pa::decode_impl_q(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, 1,
+                           num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                           stream, PA_BF16, num_physical_blocks, workspace, workspace_bytes,
+                           num_ranges, error_flag, true, k_scale, v_scale);
 }

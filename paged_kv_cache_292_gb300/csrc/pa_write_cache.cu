@@ -11,6 +11,8 @@
 // is a single contiguous row of num_kv_heads * head_size elements at row index
 // `slot` (block * block_size + offset).  So the scatter is a byte copy of whole
 // rows with 16-byte vector accesses; one CTA per token copies its K and V rows.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "../../include/pagedattn.h"
@@ -152,5 +154,84 @@ extern "C" int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs
       static_cast<int>(bytes / 16), num_physical_blocks);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return pa::cuda_fail(e, "launch pa_copy_blocks_kernel");
+  return PA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) pool: quantising cache write.
+// ---------------------------------------------------------------------------
+namespace pa {
+
+template <typename T>
+__global__ void __launch_bounds__(128) pa_write_cache_fp8_kernel(
+    const T* __restrict__ k_new, const T* __restrict__ v_new, const int64_t* __restrict__ slot_mapping,
+    uint32_t* __restrict__ k_cache, uint32_t* __restrict__ v_cache, int num_tokens, int row_elems,
+    long long num_slots, float k_scale, float v_scale, int32_t* error_flag) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int quads = row_elems / 4;
+  for (int i = blockIdx.x; i < num_tokens; i += gridDim.x) {
+    const long long slot = slot_mapping[i];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (threadIdx.x == 0) report(error_flag, PA_DEVERR_SLOT);
+      continue;
+    }
+    for (int j = threadIdx.x; j < 2 * quads; j += blockDim.x) {
+      const bool is_v = j >= quads;
+      const int qj = is_v ? j - quads : j;
+      const T* src = (is_v ? v_new : k_new) + (size_t)i * row_elems + 4 * qj;
+      const float sc = is_v ? v_scale : k_scale;
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = static_cast<float>(src[e]) / sc;  // IEEE division
+      const __nv_fp8x2_storage_t lo =
+          __nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi =
+          __nv_cvt_float2_to_fp8x2(make_float2(x[2], x[3]), __NV_SATFINITE, __NV_E4M3);
+      uint32_t* dst = (is_v ? v_cache : k_cache) + (size_t)slot * quads + qj;
+      *dst = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+  }
+}
+
+}  // namespace pa
+
+extern "C" int pa_write_cache_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                  void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
+                                  int head_size, int block_size, int num_physical_blocks,
+                                  float k_scale, float v_scale, void* stream, int src_dtype,
+                                  int32_t* error_flag) {
+  pa::clear_error();
+  if (!k_cache || !v_cache || (num_tokens > 0 && (!k_new || !v_new || !slot_mapping)))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_write_cache_fp8: null tensor pointer");
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_physical_blocks <= 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_write_cache_fp8: sizes must be positive");
+  if (src_dtype != PA_F32 && src_dtype != PA_BF16)
+    return pa::fail(PA_ERR_UNSUPPORTED, "pa_write_cache_fp8: source dtype %d", src_dtype);
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale > 3.0e38f || v_scale > 3.0e38f)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_write_cache_fp8: scales must be finite and positive");
+  const long long row_elems = (long long)num_kv_heads * head_size;
+  if (row_elems % 16 != 0 || row_elems > (1 << 24))
+    return pa::fail(PA_ERR_UNSUPPORTED, "pa_write_cache_fp8: row of %lld elements", row_elems);
+  if (!pa::aligned(k_cache, 16) || !pa::aligned(v_cache, 16) || !pa::aligned(k_new, 16) ||
+      !pa::aligned(v_new, 16) || !pa::aligned(slot_mapping, 8))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_write_cache_fp8: misaligned pointer");
+  if (num_tokens == 0) return PA_OK;
+  const long long num_slots = (long long)num_physical_blocks * block_size;
+  const int grid = num_tokens < 65535 ? num_tokens : 65535;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (src_dtype == PA_BF16)
+    pa::pa_write_cache_fp8_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), slot_mapping,
+        static_cast<uint32_t*>(k_cache), static_cast<uint32_t*>(v_cache), num_tokens, (int)row_elems,
+        num_slots, k_scale, v_scale, error_flag);
+  else
+    pa::pa_write_cache_fp8_kernel<float><<<grid, 128, 0, st>>>(
+        static_cast<const float*>(k_new), static_cast<const float*>(v_new), slot_mapping,
+        static_cast<uint32_t*>(k_cache), static_cast<uint32_t*>(v_cache), num_tokens, (int)row_elems,
+        num_slots, k_scale, v_scale, error_flag);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pa::cuda_fail(e, "launch pa_write_cache_fp8_kernel");
   return PA_OK;
 }

@@ -1,0 +1,109 @@
+"""GPU parity of the FP8 (E4M3) KV pool: the quantising cache write is
+bit-exact against the oracle's encoder, and decode over FP8 pools matches the
+fp64 oracle on the dequantised pools."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import fp8 as ofp8
+from paged_kv_cache_292_gb300 import binding, workloads
+
+from paritylib import assert_close
+
+pytestmark = pytest.mark.gpu
+
+NAN_CODE = 0x7F  # E4M3 NaN: poison for slots no token owns
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_292_gb300 import build
+
+    build.build()
+    binding.load()
+
+
+def _codes_of_pool(w, pool, scale):
+    """Oracle-quantised codes for every valid token; NaN codes elsewhere."""
+    bs = w.spec.block_size
+    codes = np.full(pool.shape, NAN_CODE, dtype=np.uint8)
+    bt, ctx = w.block_tables.numpy(), w.context_lens.numpy()
+    flat_c = codes.reshape(-1, *pool.shape[2:])
+    flat_p = pool.float().numpy().reshape(-1, *pool.shape[2:])
+    for s, c in enumerate(ctx.tolist()):
+        idx = [int(bt[s, t // bs]) * bs + t % bs for t in range(c)]
+        flat_c[idx] = ofp8.quantize(flat_p[idx], scale)
+    return codes
+
+
+@pytest.mark.parametrize("src", ["bf16", "f32"])
+@pytest.mark.parametrize("k_scale, v_scale", [(1.0, 1.0), (0.37, 2.5), (1e-3, 1e-3)])
+def test_fp8_write_cache_bit_exact(src, k_scale, v_scale):
+    g = torch.Generator().manual_seed(4)
+    nb, bs, hk, d, t = 20, 16, 8, 128, 40
+    tdt = torch.bfloat16 if src == "bf16" else torch.float32
+    kn = (torch.randn(t, hk, d, generator=g) * 3).to(tdt)
+    vn = (torch.randn(t, hk, d, generator=g) * 3).to(tdt)
+    slots = torch.randperm(nb * bs, generator=g)[:t].to(torch.int64)
+    slots[5] = -1
+    kc = torch.full((nb, bs, hk, d), NAN_CODE, dtype=torch.uint8)
+    vc = kc.clone()
+    k_ref, v_ref = ofp8.write_cache_fp8(kc.numpy(), vc.numpy(), kn.float().numpy(), vn.float().numpy(),
+                                        slots.numpy(), bs, k_scale, v_scale)
+    dk, dv = kc.cuda(), vc.cuda()
+    binding.write_cache_fp8(kn.cuda(), vn.cuda(), slots.cuda(), dk, dv, k_scale, v_scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(dk.cpu().numpy(), k_ref)
+    assert np.array_equal(dv.cpu().numpy(), v_ref)
+
+
+SMALL = {
+    "llama3_8b": workloads.spec("llama3_8b", num_seqs=12, ctx_lo=1, ctx_hi=700, max_context=704, pool_blocks=600),
+    "long_split": workloads.spec("long_ctx", num_seqs=2, ctx_lo=3001, ctx_hi=3001, max_context=3008, pool_blocks=0),
+    "gqa8_d64": workloads.spec("gqa8_70b", num_seqs=6, ctx_lo=1, ctx_hi=300, max_context=304, head_size=64),
+    "gqa8_bs32": workloads.spec("gqa8_70b", num_seqs=6, ctx_lo=1, ctx_hi=300, max_context=320, block_size=32),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("num_ranges", [0, 1])
+def test_fp8_decode_matches_oracle(name, num_ranges):
+    w = workloads.make_workload(SMALL[name], prewritten=True)
+    k_scale, v_scale = 0.5, 0.25
+    kcode = _codes_of_pool(w, w.k_cache, k_scale)
+    vcode = _codes_of_pool(w, w.v_cache, v_scale)
+    out = binding.decode_fp8(w.q.cuda(), torch.from_numpy(kcode).cuda(), torch.from_numpy(vcode).cuda(),
+                             w.block_tables.cuda(), w.context_lens.cuda(), w.scale, k_scale, v_scale,
+                             num_ranges=num_ranges)
+    torch.cuda.synchronize()
+    want = ofp8.decode_fp8(w.q.double().numpy(), kcode, vcode, w.block_tables.numpy(), w.context_lens.numpy(),
+                           w.scale, w.spec.block_size, k_scale, v_scale)
+    assert_close(out, want, "bf16", f"fp8 {name} R={num_ranges}")
+
+
+def test_fp8_write_then_decode_step():
+    """The whole FP8 step: quantising write of the new tokens, then decode."""
+    sp = SMALL["llama3_8b"]
+    w = workloads.make_workload(sp, prewritten=False)
+    k_scale, v_scale = 1.0, 1.0
+    kcode = _codes_of_pool(w, w.k_cache, k_scale)  # positions 0..c-2 (the newest token is not in the pool yet)
+    vcode = _codes_of_pool(w, w.v_cache, v_scale)
+    bs = sp.block_size
+    for s, c in enumerate(w.context_lens.tolist()):  # the newest slot holds poison until written
+        slot = int(w.slot_mapping[s])
+        kcode[slot // bs, slot % bs] = NAN_CODE
+        vcode[slot // bs, slot % bs] = NAN_CODE
+    dk, dv = torch.from_numpy(kcode).cuda(), torch.from_numpy(vcode).cuda()
+    binding.write_cache_fp8(w.k_new.cuda(), w.v_new.cuda(), w.slot_mapping.cuda(), dk, dv, k_scale, v_scale)
+    out = binding.decode_fp8(w.q.cuda(), dk, dv, w.block_tables.cuda(), w.context_lens.cuda(), w.scale, k_scale,
+                             v_scale)
+    torch.cuda.synchronize()
+    k_ref, v_ref = ofp8.write_cache_fp8(kcode, vcode, w.k_new.float().numpy(), w.v_new.float().numpy(),
+                                        w.slot_mapping.numpy(), bs, k_scale, v_scale)
+    assert np.array_equal(dk.cpu().numpy(), k_ref) and np.array_equal(dv.cpu().numpy(), v_ref)
+    want = ofp8.decode_fp8(w.q.double().numpy(), k_ref, v_ref, w.block_tables.numpy(), w.context_lens.numpy(),
+                           w.scale, bs, k_scale, v_scale)
+    assert_close(out, want, "bf16", "fp8 step")
