@@ -316,6 +316,19 @@ def run_ours(args):
         extra = (Q - 1) * S * (2 * H * D * e_ + 2 * 2 * Hk * D * e_ + 8)
         by = dict(by, decode=by["decode"] + (Q - 1) * 2 * S * H * D * e_)
         by["step"] += extra
+    fp8 = args.kv == "fp8"
+    if fp8:
+        if Q > 1 or sp.dtype != "bf16":
+            raise SystemExit("--kv fp8 needs bf16 and one query per sequence")
+        # E4M3 pools (one scale per pool); the prompt's K/V quantised once here.
+        k_scale = v_scale = 1.0
+        g["k_cache"] = (g["k_cache"].float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+        g["v_cache"] = (g["v_cache"].float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+        e_kv = Hk * D * 2  # per token: K+V bytes saved by one-byte elements
+        ctx_tok = int(w.context_lens.sum())
+        by = dict(by, decode=by["decode"] - ctx_tok * e_kv, kv_logical=by["kv_logical"] // 2)
+        by["write"] -= S * 2 * Hk * D  # the write stores one byte per element instead of two
+        by["step"] = by["decode"] + by["write"]
     n_new = S * Q
     out = torch.empty_like(g["q"])
     stream = torch.cuda.current_stream(dev)
@@ -326,13 +339,21 @@ def run_ours(args):
     P = binding._ptr
 
     def write(gg, sh=sh):
-        rc = lib.pa_write_cache(P(gg["k_new"]), P(gg["v_new"]), P(gg["slot_mapping"]), P(g["k_cache"]),
-                                P(g["v_cache"]), n_new, Hk, D, bs, NB, sh, dt)
+        if fp8:
+            rc = lib.pa_write_cache_fp8(P(gg["k_new"]), P(gg["v_new"]), P(gg["slot_mapping"]), P(g["k_cache"]),
+                                        P(g["v_cache"]), n_new, Hk, D, bs, NB, k_scale, v_scale, sh, dt, None)
+        else:
+            rc = lib.pa_write_cache(P(gg["k_new"]), P(gg["v_new"]), P(gg["slot_mapping"]), P(g["k_cache"]),
+                                    P(g["v_cache"]), n_new, Hk, D, bs, NB, sh, dt)
         if rc:
             raise RuntimeError(binding.pa_last_error())
 
     def decode(gg, o, sh=sh):
-        if Q == 1:
+        if fp8:
+            rc = lib.pa_decode_fp8(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
+                                   P(gg["context_lens"]), S, H, Hk, D, bs, MB, w.scale, k_scale, v_scale, sh, 0,
+                                   P(ws), ws_bytes, 0, None)
+        elif Q == 1:
             rc = lib.pa_decode_ws(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
                                   P(gg["context_lens"]), S, H, Hk, D, bs, MB, w.scale, sh, dt, P(ws), ws_bytes)
         else:
@@ -445,7 +466,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if sp.dtype == "bf16" else "f32",
+        "dtype": "fp8_e4m3" if fp8 else ("bf16" if sp.dtype == "bf16" else "f32"),
         "data": "synthetic (seeded N(0,1) K/V/q via PCG64, cast RNE to bf16; shuffled block pool)",
         "config": {
             "workload": args.workload,
@@ -456,6 +477,7 @@ def run_ours(args):
                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
             "replicas": world,
             "queries_per_seq": Q,
+            "kv_pool": "fp8_e4m3" if fp8 else sp.dtype,
             "launch": "CUDA graph replay" if args.graph else "eager (programmatic dependent launch)",
         },
         "roofline": {
@@ -615,6 +637,8 @@ def main():
     ap.add_argument("--block-size", type=int, default=None, help="override the workload's block size")
     ap.add_argument("--queries", type=int, default=1,
                     help="query tokens per sequence (several: causal multi-query step via pa_decode_mq)")
+    ap.add_argument("--kv", choices=["native", "fp8"], default="native",
+                    help="KV pool element type: the workload's own, or E4M3 FP8 (quantising write + FP8 decode)")
     ap.add_argument("--loop", action="store_true",
                     help="steady-state decode loop driven by the host block manager (separate metric)")
     args = ap.parse_args()
