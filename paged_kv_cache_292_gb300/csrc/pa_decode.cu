@@ -33,6 +33,8 @@
 //     out = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i.  The ticket counters
 //     are reset by that warp, so the scratch is left zeroed for the next call.
 //   * Empty sequences get a zero row from the prologue.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <float.h>
@@ -50,7 +52,8 @@ namespace pa {
 
 constexpr int kMaxGroupHeads = 8;  // KV heads per CTA (one consumer warp each)
 constexpr int kMaxQueryGroup = 8;  // query heads per KV head (MMA N extent)
-constexpr int kRowSkew = 16;       // bytes between staged rows beyond the row itself
+constexpr int kRowSkew = 16;       // fp32 stages: bytes between staged rows beyond the row itself
+constexpr uint32_t kLine = 128;    // tensor-core stages: bytes per swizzled line
 constexpr int kMaxRowBytes = 2048;  // bytes of one staged token row (K or V)
 constexpr int kMaxRanges = 4096;    // bounds the partial-result scratch
 
@@ -67,6 +70,7 @@ struct StageMeta {
 };
 
 struct DecodeParams {
+  CUtensorMap tm_k, tm_v;  // tensor-core paths: 4-D views of the pools (see make_tensor_maps)
   void* out;
   const void* q;
   const void* k_cache;
@@ -86,7 +90,10 @@ struct DecodeParams {
   int num_queries;  // query tokens per sequence (1 for plain decode)
   float v_scale;    // FP8 pools: value of a V code is decode(code) * v_scale (else 1)
   uint32_t row_bytes, pitch, q_bytes, stage_bytes;
-  float scale_log2;  // scale * log2(e)
+  uint32_t lines;      // tensor-core stages: 128-byte lines per staged token row
+  uint32_t box_rows;   // token rows per tensor copy: gcd(block_size, 16)
+  uint32_t box_bytes;  // bytes one tensor copy lands (box_rows * lines * 128)
+  float scale_log2;    // scale * log2(e)
 };
 
 struct Layout {
@@ -94,7 +101,10 @@ struct Layout {
 };
 
 // Shared-memory carve-up; identical on host (sizing) and device (addressing).
-PA_HD Layout make_layout(int stages, int q_slots, uint32_t q_bytes, uint32_t stage_bytes) {
+// Swizzled (tensor-core) stages start on a 1 KiB boundary of the shared
+// window, for which `total` keeps 1 KiB of slack.
+PA_HD Layout make_layout(int stages, int q_slots, uint32_t q_bytes, uint32_t stage_bytes,
+                         bool swizzled) {
   Layout L;
   uint32_t o = 0;
   L.bar = o;
@@ -109,7 +119,7 @@ PA_HD Layout make_layout(int stages, int q_slots, uint32_t q_bytes, uint32_t sta
   o += q_slots * ((q_bytes + 127u) & ~127u);
   o = (o + 127u) & ~127u;
   L.stage = o;
-  o += stages * stage_bytes;
+  o += stages * stage_bytes + (swizzled ? 1024u : 0u);
   L.total = o;
   return L;
 }
@@ -144,6 +154,32 @@ __device__ __forceinline__ long long warp_incl_scan_ll(long long v, int lane) {
 // query heads; D = head size.
 // ---------------------------------------------------------------------------
 
+// Stages of the tensor-core consumers.  A K or V half-stage holds the tile's
+// 16 token rows, row r as `lines` 128-byte lines (the head group's bytes,
+// then zero-filled lines up to an odd count or the count a copy's alignment
+// needs), written by tensor copies with the 128-byte swizzle: line
+// L = r * lines + chunk stores its 16-byte unit u at position u ^ (L % 8).
+// With `lines` odd, one unit of 8 consecutive rows lands in 8 different bank
+// groups, so ldmatrix reads are conflict-free.
+//
+// RowPtr<NC> holds one lane's ldmatrix row address for a head whose bytes
+// span NC 128-byte chunks: units u0 + 2j (j = 0, 1, ...) of row r, where u0
+// counts 16-byte units from the start of the group's row and has bits 1-2
+// clear, so stepping j within a chunk flips address bits 5-6 only.
+template <int NC>
+struct RowPtr {
+  uint32_t a[NC];
+  __device__ __forceinline__ RowPtr(uint32_t half, int r, int u0, uint32_t lines) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const uint32_t unit = (uint32_t)u0 + 8u * c;
+      const uint32_t L = (uint32_t)r * lines + (unit >> 3);
+      a[c] = half + L * kLine + (((unit & 7u) ^ (L & 7u)) << 4);
+    }
+  }
+  __device__ __forceinline__ uint32_t at(int j) const { return a[j >> 2] ^ ((uint32_t)(j & 3) << 5); }
+};
+
 // bf16 tensor-core consumer.  Lane l owns query heads hA = 2*(l%4), hB = hA+1
 // (columns of the score fragment) and, per 16-wide slice mt of the head
 // dimension, output dims mt*16 + l/4 and +8.
@@ -175,15 +211,19 @@ struct MmaConsumer {
     l_a = l_b = 0.f;
   }
 
-  __device__ __forceinline__ void tile(uint32_t k_base, uint32_t v_base, uint32_t pitch,
+  static constexpr int NC = D * 2 > 128 ? D * 2 / 128 : 1;  // 128-byte chunks per head
+
+  // k_half / v_half: the stage's K and V halves; uh: first 16-byte unit of
+  // this warp's head within the group's row.
+  __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
                                        int nvalid, float scale_log2, int lane) {
     // S^T = K_tile * Q^T : rows = tokens, columns = query heads.
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t k_lane = k_base + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 16;
+    const RowPtr<NC> kp(k_half, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
-      ldmatrix_x4(a, k_lane + ks * 32);
+      ldmatrix_x4(a, kp.at(ks));
       if (ks & 1)
         mma_bf16_16816(c1, a, qb[ks][0], qb[ks][1]);
       else
@@ -225,7 +265,7 @@ struct MmaConsumer {
     const uint32_t rb1 = movmatrix_trans(r_bot);
 
     // O^T += V^T * P^T : rows = head dims, columns = query heads.
-    const uint32_t v_lane = v_base + ((lane & 7) + (lane >> 4) * 8) * pitch + ((lane >> 3) & 1) * 16;
+    const RowPtr<NC> vp(v_half, (lane & 7) + (lane >> 4) * 8, uh + ((lane >> 3) & 1), lines);
     const int t2 = 2 * (lane & 3);
     uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
     if (nvalid < kTile) {
@@ -237,7 +277,7 @@ struct MmaConsumer {
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       uint32_t a[4];
-      ldmatrix_x4_trans(a, v_lane + mt * 32);
+      ldmatrix_x4_trans(a, vp.at(mt));
       a[0] &= keep_lo;
       a[1] &= keep_lo;
       a[2] &= keep_hi;
@@ -341,7 +381,9 @@ struct MmaConsumerMQ {
     }
   }
 
-  __device__ __forceinline__ void tile(uint32_t k_base, uint32_t v_base, uint32_t pitch,
+  static constexpr int NC = D * 2 > 128 ? D * 2 / 128 : 1;
+
+  __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
                                        int nvalid, int tok0, int ctx, int G, int Q,
                                        float scale_log2, int lane) {
     float c[NT][4];
@@ -349,11 +391,11 @@ struct MmaConsumerMQ {
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
-    const uint32_t k_lane = k_base + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 16;
+    const RowPtr<NC> kp(k_half, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
-      ldmatrix_x4(a, k_lane + ks * 32);
+      ldmatrix_x4(a, kp.at(ks));
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(c[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
     }
@@ -400,7 +442,7 @@ struct MmaConsumerMQ {
       rb0[nt] = movmatrix_trans(r_top);
       rb1[nt] = movmatrix_trans(r_bot);
     }
-    const uint32_t v_lane = v_base + ((lane & 7) + (lane >> 4) * 8) * pitch + ((lane >> 3) & 1) * 16;
+    const RowPtr<NC> vp(v_half, (lane & 7) + (lane >> 4) * 8, uh + ((lane >> 3) & 1), lines);
     const int t2 = 2 * (lane & 3);
     uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
     if (nvalid < kTile) {
@@ -410,7 +452,7 @@ struct MmaConsumerMQ {
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       uint32_t a[4];
-      ldmatrix_x4_trans(a, v_lane + mt * 32);
+      ldmatrix_x4_trans(a, vp.at(mt));
       a[0] &= keep_lo;
       a[1] &= keep_lo;
       a[2] &= keep_hi;
@@ -475,12 +517,16 @@ struct MmaConsumerMQ {
 
 // Consumer for an FP8 (E4M3) pool with bf16 queries and outputs.  Codes are
 // widened to f16 in registers (exact) and both products run on f16 MMAs.
-// Q.K: as in MmaConsumer, K fragments come from 16-bit shared loads (two
-// codes of adjacent head dims).  P.V: the MMA's output rows are permuted so
-// that lane l/4 owns the adjacent dims 2*(l/4) and +1 of each 16-wide slice:
-// each A register then pairs one dim of two tokens, built from two 16-bit
-// loads with a byte permute.  Scores carry k_scale in scale_log2; v_scale is
-// applied to the finished output.
+// Shared-memory reads use ldmatrix on 16-bit units (two codes each):
+//   Q.K  - the order of head dims inside each 16-wide k-step is permuted so
+//          that lane t's four consecutive codes (dims 4t..4t+3) are its k
+//          pairs (2t, 2t+1) and (2t+8, 2t+9); the query fragment is loaded in
+//          the same order, so the sum is unchanged.
+//   P.V  - ldmatrix.trans hands each lane two dims of two tokens; the MMA's
+//          output rows are permuted so that lane l/4 owns dims 2*(l/4) and
+//          +1 of each 16-wide slice, and one byte permute per register builds
+//          the (token, token) pairs the A operand needs.
+// Scores carry k_scale in scale_log2; v_scale is applied to the output.
 template <int D>
 struct MmaConsumerF8 {
   static constexpr int KS = D / 16;
@@ -490,16 +536,15 @@ struct MmaConsumerF8 {
 
   __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G,
                                                 int lane) {
-    const int n = lane >> 2, t2 = 2 * (lane & 3);
+    const int n = lane >> 2, t4 = 4 * (lane & 3);
     const __nv_bfloat16* qh =
         reinterpret_cast<const __nv_bfloat16*>(qslot) + (size_t)(w * G + n) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       if (n < G) {
-        const uint32_t lo = *reinterpret_cast<const uint32_t*>(qh + ks * 16 + t2);
-        const uint32_t hi = *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 8 + t2);
-        qb[ks][0] = pack_f16x2(bf16_lo(lo), bf16_hi(lo));
-        qb[ks][1] = pack_f16x2(bf16_lo(hi), bf16_hi(hi));
+        const uint2 v = *reinterpret_cast<const uint2*>(qh + ks * 16 + t4);  // dims t4 .. t4+3
+        qb[ks][0] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));  // k pair (2t, 2t+1)
+        qb[ks][1] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));  // k pair (2t+8, 2t+9)
       } else {
         qb[ks][0] = 0u;
         qb[ks][1] = 0u;
@@ -511,24 +556,33 @@ struct MmaConsumerF8 {
     l_a = l_b = 0.f;
   }
 
-  __device__ __forceinline__ void tile(const unsigned char* k_base, const unsigned char* v_base,
-                                       uint32_t pitch, int nvalid, float scale_log2, int lane) {
-    const int g = lane >> 2, t2 = 2 * (lane & 3);
+  __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
+                                       int nvalid, float scale_log2, int lane) {
+    // Matrices of one ldmatrix.x4: (rows 0-7, bytes 0-15), (rows 8-15, 0-15),
+    // (rows 0-7, 16-31), (rows 8-15, 16-31) - two k-steps / m-tiles of 16 dims.
+    const int r = (lane & 7) + ((lane >> 3) & 1) * 8, u0 = uh + (lane >> 4);
+    const RowPtr<1> kp(k_half, r, u0, lines), vp(v_half, r, u0, lines);
+    uint32_t kr[KS / 2][4], vr[KS / 2][4];
+#pragma unroll
+    for (int j = 0; j < KS / 2; ++j) ldmatrix_x4(kr[j], kp.at(j));
+#pragma unroll
+    for (int j = 0; j < KS / 2; ++j) ldmatrix_x4_trans(vr[j], vp.at(j));
+
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    const unsigned char* k_r0 = k_base + g * pitch;
-    const unsigned char* k_r1 = k_base + (g + 8) * pitch;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
+      const uint32_t top = kr[ks >> 1][2 * (ks & 1)], bot = kr[ks >> 1][2 * (ks & 1) + 1];
       uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2(*reinterpret_cast<const unsigned short*>(k_r0 + ks * 16 + t2));
-      a[1] = e4m3x2_to_f16x2(*reinterpret_cast<const unsigned short*>(k_r1 + ks * 16 + t2));
-      a[2] = e4m3x2_to_f16x2(*reinterpret_cast<const unsigned short*>(k_r0 + ks * 16 + 8 + t2));
-      a[3] = e4m3x2_to_f16x2(*reinterpret_cast<const unsigned short*>(k_r1 + ks * 16 + 8 + t2));
+      a[0] = e4m3x2_to_f16x2(top);        // token row g: codes 0,1
+      a[1] = e4m3x2_to_f16x2(bot);        // token row g+8
+      a[2] = e4m3x2_to_f16x2(top >> 16);  // codes 2,3
+      a[3] = e4m3x2_to_f16x2(bot >> 16);
       if (ks & 1)
         mma_f16_16816(c1, a, qb[ks][0], qb[ks][1]);
       else
         mma_f16_16816(c0, a, qb[ks][0], qb[ks][1]);
     }
+    const int g = lane >> 2, t2 = 2 * (lane & 3);
     float s0 = (c0[0] + c1[0]) * scale_log2, s1 = (c0[1] + c1[1]) * scale_log2;
     float s2 = (c0[2] + c1[2]) * scale_log2, s3 = (c0[3] + c1[3]) * scale_log2;
     if (g >= nvalid) s0 = s1 = -INFINITY;
@@ -554,24 +608,22 @@ struct MmaConsumerF8 {
     l_b = l_b * alpha_b + p1 + p3;
     const uint32_t pb0 = movmatrix_trans(p_top), pb1 = movmatrix_trans(p_bot);
     const uint32_t rb0 = movmatrix_trans(r_top), rb1 = movmatrix_trans(r_bot);
-    // V rows of this lane's tokens; rows past the end read as code 0 (+0.0).
-    const bool ok0 = t2 < nvalid, ok1 = t2 + 1 < nvalid, ok8 = t2 + 8 < nvalid, ok9 = t2 + 9 < nvalid;
-    const unsigned char* v0 = v_base + t2 * pitch;
-    const unsigned char* v1 = v0 + pitch;
-    const unsigned char* v8 = v_base + (t2 + 8) * pitch;
-    const unsigned char* v9 = v8 + pitch;
+    // Each V register holds bytes (tok 2t: dim 2g, 2g+1 | tok 2t+1: dim 2g, 2g+1);
+    // tokens past the end are zeroed (code 0 is +0.0) before they meet a weight.
+    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+    if (nvalid < kTile) {
+      keep_lo = (t2 < nvalid ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid ? 0xffff0000u : 0u);
+      keep_hi = (t2 + 8 < nvalid ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid ? 0xffff0000u : 0u);
+    }
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
-      const int dd = mt * 16 + 2 * g;  // this lane's dims dd, dd + 1
-      const uint32_t w0 = ok0 ? *reinterpret_cast<const unsigned short*>(v0 + dd) : 0u;
-      const uint32_t w1 = ok1 ? *reinterpret_cast<const unsigned short*>(v1 + dd) : 0u;
-      const uint32_t w8 = ok8 ? *reinterpret_cast<const unsigned short*>(v8 + dd) : 0u;
-      const uint32_t w9 = ok9 ? *reinterpret_cast<const unsigned short*>(v9 + dd) : 0u;
+      const uint32_t top = vr[mt >> 1][2 * (mt & 1)] & keep_lo;      // tokens 2t, 2t+1
+      const uint32_t bot = vr[mt >> 1][2 * (mt & 1) + 1] & keep_hi;  // tokens 2t+8, 2t+9
       uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2(__byte_perm(w0, w1, 0x0040));  // dim dd, tokens t2, t2+1
-      a[1] = e4m3x2_to_f16x2(__byte_perm(w0, w1, 0x0051));  // dim dd+1
-      a[2] = e4m3x2_to_f16x2(__byte_perm(w8, w9, 0x0040));  // dim dd, tokens t2+8, t2+9
-      a[3] = e4m3x2_to_f16x2(__byte_perm(w8, w9, 0x0051));
+      a[0] = e4m3x2_to_f16x2(__byte_perm(top, 0u, 0x0020));  // dim 2g: tokens 2t, 2t+1
+      a[1] = e4m3x2_to_f16x2(__byte_perm(top, 0u, 0x0031));  // dim 2g+1
+      a[2] = e4m3x2_to_f16x2(__byte_perm(bot, 0u, 0x0020));
+      a[3] = e4m3x2_to_f16x2(__byte_perm(bot, 0u, 0x0031));
       acc[mt][0] *= alpha_a;
       acc[mt][1] *= alpha_b;
       acc[mt][2] *= alpha_a;
@@ -872,14 +924,15 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 // sequence with a causal mask, (query, head) columns in one / two MMA N-tiles.
 template <typename T, int D, int GMAX, int QMODE, bool KV8 = false>
 __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
-    pa_decode_kernel(const DecodeParams p) {
+    pa_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
   const int HG = p.num_head_groups, R = p.num_ranges, S = p.num_seqs;
   const int r = blockIdx.x / HG, hg = blockIdx.x % HG;
   const int Hg = p.heads_per_cta;
-  const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes);
+  constexpr bool kMmaPath = (sizeof(T) == 2);  // tensor-core consumers, swizzled stages
+  const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes, kMmaPath);
   long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
   griddep_wait();  // inputs may come from the kernel just before (e.g. the cache write)
 
@@ -947,7 +1000,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const long long p_first = misc[33];
   const uint32_t q_slot_bytes = (p.q_bytes + 127u) & ~127u;
   const uint32_t qring = smem_addr(smem + L.qring);
-  const uint32_t stages = smem_addr(smem + L.stage);
+  const uint32_t stages =
+      kMmaPath ? ((smem_addr(smem + L.stage) + 1023u) & ~1023u) : smem_addr(smem + L.stage);
   const int G = p.group, H = p.num_heads, Hk = p.num_kv_heads, bs = p.block_size;
 
   if (warp == Hg) {
@@ -968,6 +1022,10 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     uint32_t ph = 0, qph = 0;
     const int t = lane & 15;
     const bool is_v = lane >= 16;
+    if (kMmaPath && lane == 0) {
+      prefetch_tensormap(&p.tm_k);
+      prefetch_tensormap(&p.tm_v);
+    }
     // Block-table window of the current sequence: lane i holds entry cb+i in
     // `cur` and cb+32+i in `nxt`.  The window slides one chunk at a time and the
     // next chunk is loaded a chunk ahead, so lookups never wait on memory except
@@ -1046,6 +1104,11 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         report(p.error_flag, PA_DEVERR_BLOCK_ID);
         ok = false;
       }
+      // Tensor-core paths: lane t (t a multiple of box_rows) copies tile rows
+      // t .. t + box_rows - 1, which lie in one block, as one tensor box; rows
+      // past the context in that block come along and are masked by the
+      // consumers.  fp32: one bulk copy per valid token row.
+      if constexpr (kMmaPath) ok = ok && (t % (int)p.box_rows) == 0;
       const unsigned copies = __ballot_sync(0xffffffffu, ok);
       if (!mbar_wait(empty_bar(st), ph ^ 1u)) {
         report(p.error_flag, PA_DEVERR_TIMEOUT);
@@ -1053,14 +1116,21 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       }
       if (lane == 0) {
         meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, c, 0};
-        mbar_arrive_expect_tx(full_bar(st), __popc(copies) * p.row_bytes);
+        mbar_arrive_expect_tx(full_bar(st), __popc(copies) * (kMmaPath ? p.box_bytes : p.row_bytes));
       }
       __syncwarp();
       if (ok) {
-        const size_t row = ((size_t)phys * bs + tok % bs) * Hk + (size_t)hg * Hg;
-        const KV* src = (is_v ? vc : kc) + row * D;
-        const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
-        bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
+        if constexpr (kMmaPath) {
+          const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.lines * kLine : 0u) +
+                               t * p.lines * kLine;
+          tma_load_4d(dst, is_v ? &p.tm_v : &p.tm_k, 0, 0, hg, (int)(phys * bs + tok % bs),
+                      full_bar(st));
+        } else {
+          const size_t row = ((size_t)phys * bs + tok % bs) * Hk + (size_t)hg * Hg;
+          const KV* src = (is_v ? vc : kc) + row * D;
+          const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
+          bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
+        }
       }
       if (++st == NS) {
         st = 0;
@@ -1100,16 +1170,17 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
           qph ^= 1u;
         }
       }
-      constexpr uint32_t kKVBytes = KV8 ? 1u : (uint32_t)sizeof(T);
-      const uint32_t k_base = stages + st * p.stage_bytes + w * D * kKVBytes;
-      const uint32_t v_base = k_base + kTile * p.pitch;
+      constexpr int kKVBytes = KV8 ? 1 : (int)sizeof(T);
+      const uint32_t k_half = stages + st * p.stage_bytes;
+      const uint32_t v_half = k_half + kTile * p.lines * kLine;
+      const int uh = w * D * kKVBytes / 16;  // this head's first 16-byte unit in the row
       if constexpr (KV8) {
-        const unsigned char* kb = smem + L.stage + st * p.stage_bytes + w * D;
-        cons.tile(kb, kb + kTile * p.pitch, p.pitch, mt.nvalid, p.scale_log2, lane);
+        cons.tile(k_half, v_half, p.lines, uh, mt.nvalid, p.scale_log2, lane);
       } else if constexpr (kMma && QMODE > 0) {
-        cons.tile(k_base, v_base, p.pitch, mt.nvalid, mt.tok0, mt.ctx, G, p.num_queries, p.scale_log2, lane);
+        cons.tile(k_half, v_half, p.lines, uh, mt.nvalid, mt.tok0, mt.ctx, G, p.num_queries,
+                  p.scale_log2, lane);
       } else if constexpr (kMma) {
-        cons.tile(k_base, v_base, p.pitch, mt.nvalid, p.scale_log2, lane);
+        cons.tile(k_half, v_half, p.lines, uh, mt.nvalid, p.scale_log2, lane);
       } else {
         const unsigned char* kb = smem + L.stage + st * p.stage_bytes + w * D * sizeof(T);
         cons.tile(kb, kb + kTile * p.pitch, p.pitch, mt.nvalid, p.scale_log2, G, lane);
@@ -1140,6 +1211,7 @@ namespace {
 struct Plan {
   int Hg, HG, R, stages, q_slots;
   uint32_t row_bytes, pitch, q_bytes, stage_bytes, smem;
+  uint32_t lines, box_rows, box_bytes;  // tensor-core paths (see DecodeParams)
   size_t ws_ml, ws_o, ws_partials, ws_counters, ws_total;
 };
 
@@ -1177,22 +1249,55 @@ int default_ranges(const DeviceInfo& dev, int HG) {
   return r < 1 ? 1 : r;
 }
 
+int gcd_int(int a, int b) {
+  while (b != 0) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// elt: bytes of a pool element; q_elt: bytes of a query element (bf16 queries
+// select the tensor-core consumers, whose stages are swizzled tensor boxes).
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int elt,
               int num_ranges, const DeviceInfo& dev, Plan* pl, int num_queries = 1,
-              int q_elt = 0) {
-  if (q_elt == 0) q_elt = elt;  // query element size (differs from the pool's for FP8 pools)
+              int q_elt = 0, int block_size = 16) {
+  if (q_elt == 0) q_elt = elt;
   const int G = num_heads / num_kv_heads;
+  const bool mma = q_elt == 2;
   pl->Hg = heads_per_cta(num_kv_heads, head_size, elt);
   pl->HG = num_kv_heads / pl->Hg;
   pl->R = num_ranges > 0 ? num_ranges : default_ranges(dev, pl->HG);
   pl->row_bytes = (uint32_t)(pl->Hg * head_size * elt);
-  pl->pitch = pl->row_bytes + kRowSkew;
   pl->q_bytes = (uint32_t)(num_queries * pl->Hg * G * head_size * q_elt);
+  pl->lines = pl->box_rows = pl->box_bytes = 0;
+  if (mma) {
+    if (pl->row_bytes % kLine != 0)
+      return fail(PA_ERR_UNSUPPORTED,
+                  "pa_decode: %d KV heads x %d dims make %u-byte rows, not whole 128-byte lines",
+                  pl->Hg, head_size, pl->row_bytes);
+    // A tensor copy moves box_rows = gcd(block_size, 16) rows (they share a
+    // block) and must land on a 1 KiB boundary under the 128-byte swizzle, so
+    // box_rows * lines is a multiple of 8: lines is a multiple of `step`.  An
+    // odd multiple spreads consecutive rows over the most bank groups.
+    const uint32_t chunks = pl->row_bytes / kLine;
+    const int br = gcd_int(block_size, kTile);
+    const uint32_t step = 8u / (uint32_t)gcd_int(br, 8);
+    uint32_t lines = (chunks + step - 1) / step * step;
+    if ((lines / step) % 2 == 0) lines += step;
+    pl->lines = lines;
+    pl->box_rows = (uint32_t)br;
+    pl->box_bytes = (uint32_t)br * lines * kLine;
+    pl->pitch = lines * kLine;
+  } else {
+    pl->pitch = pl->row_bytes + kRowSkew;
+  }
   pl->stage_bytes = 2u * kTile * pl->pitch;
   pl->stages = 0;
   const int pref[][2] = {{6, 2}, {5, 2}, {4, 2}, {3, 2}, {3, 1}, {2, 2}, {2, 1}};
   for (auto& c : pref) {
-    const Layout L = make_layout(c[0], c[1], pl->q_bytes, pl->stage_bytes);
+    const Layout L = make_layout(c[0], c[1], pl->q_bytes, pl->stage_bytes, mma);
     if ((int)L.total <= dev.max_smem_optin) {
       pl->stages = c[0];
       pl->q_slots = c[1];
@@ -1257,6 +1362,55 @@ cudaError_t launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStre
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+// The pools seen by the tensor copies: 4-D byte tensors (byte within a
+// 128-byte chunk, chunk within a head group's row, head group, token row)
+// with strides (1, 128, group row bytes, token row bytes).  A box is
+// (128, lines, 1, box_rows); its lines past the group's row are outside the
+// tensor, so they arrive zero-filled without touching memory.
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_tiled_fn() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      (void)cudaGetLastError();
+      return static_cast<EncodeTiledFn>(nullptr);
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+int make_tensor_maps(DecodeParams* prm, const Plan& pl, int num_kv_heads, int head_size, int kv_elt,
+                     int block_size, int num_physical_blocks) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return fail(PA_ERR_CUDA, "pa_decode: the driver has no cuTensorMapEncodeTiled");
+  // Unknown pool size: the row extent only has to cover every valid row, and
+  // no pool that fits in device memory has 2^31 token rows of >= 128 bytes.
+  const uint64_t rows =
+      num_physical_blocks > 0 ? (uint64_t)num_physical_blocks * block_size : (1ull << 31);
+  if (rows > (1ull << 31))
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: %llu token rows in the pool (at most 2^31)",
+                (unsigned long long)rows);
+  const cuuint64_t dims[4] = {kLine, pl.row_bytes / kLine, (cuuint64_t)pl.HG, rows};
+  const cuuint64_t strides[3] = {kLine, pl.row_bytes,
+                                 (cuuint64_t)num_kv_heads * head_size * kv_elt};
+  const cuuint32_t box[4] = {kLine, pl.lines, 1u, pl.box_rows};
+  const cuuint32_t estride[4] = {1u, 1u, 1u, 1u};
+  for (int i = 0; i < 2; ++i) {
+    const CUresult r = enc(i ? &prm->tm_v : &prm->tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                           const_cast<void*>(i ? prm->v_cache : prm->k_cache), dims, strides, box,
+                           estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  }
+  return PA_OK;
 }
 
 template <typename T, int D, int GMAX, int QMODE = 0, bool KV8 = false>
@@ -1327,7 +1481,7 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   const int elt = dtype == PA_F32 ? 4 : 2;
   Plan pl{};
   rc = make_plan(num_seqs, num_heads, num_kv_heads, head_size, kv_fp8 ? 1 : elt, num_ranges, dev, &pl,
-                 num_queries, elt);
+                 num_queries, elt, block_size);
   if (rc != PA_OK) return rc;
   int32_t* counters = nullptr;
   if (workspace == nullptr) {
@@ -1373,6 +1527,14 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   prm.pitch = pl.pitch;
   prm.q_bytes = pl.q_bytes;
   prm.stage_bytes = pl.stage_bytes;
+  prm.lines = pl.lines;
+  prm.box_rows = pl.box_rows;
+  prm.box_bytes = pl.box_bytes;
+  if (dtype == PA_BF16) {
+    rc = make_tensor_maps(&prm, pl, num_kv_heads, head_size, kv_fp8 ? 1 : 2, block_size,
+                          num_physical_blocks);
+    if (rc != PA_OK) return rc;
+  }
   prm.scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
   prm.v_scale = v_scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -27,19 +27,13 @@ __device__ __forceinline__ void mbar_init_fence() {
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  uint64_t state;
-  asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(bar) : "memory");
-  (void)state;
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Arrive once and raise the barrier's expected transaction bytes.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  uint64_t state;
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
-               : "=l"(state)
-               : "r"(bar), "r"(bytes)
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
-  (void)state;
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -83,6 +77,22 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
           dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Tiled tensor copy (TMA) of one 4-D box into shared memory; `tmap` is the
+// generic address of a tensor map held in kernel-parameter space.  The box
+// lands densely (innermost coordinate fastest), swizzled as the map says.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                            int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
 // ---- warp-level matrix data movement -------------------------------------
