@@ -14,12 +14,15 @@
 //   * The flattened tile list of the batch is cut into equal ranges (see
 //     pa_schedule.h), so every CTA moves the same K/V bytes.
 //   * Warp `Hg` (the producer) walks the range tile by tile.  For each tile of
-//     16 tokens it looks up the block ids, then issues one bulk copy per token
-//     row of K and of V: a row is all `Hg` KV heads of the token, contiguous in
-//     the pool ([block, slot, head, dim] layout), e.g. 2 KiB for 8 heads x 128
-//     x bf16.  Rows land `pitch = row + 16` bytes apart so that ldmatrix reads
-//     of 8 consecutive tokens hit distinct banks.  Each sequence's query slice
-//     is copied once into a small ring of its own.
+//     16 tokens it looks up the block ids and copies K and V into the stage.
+//     A token row is all `Hg` KV heads of the token, contiguous in the pool
+//     ([block, slot, head, dim] layout), e.g. 2 KiB for 8 heads x 128 x bf16.
+//     Tensor-core paths (bf16, FP8): one tensor-map box per run of
+//     gcd(block_size, 16) rows of one block, landing with the 128-byte
+//     swizzle in rows of an odd number of 128-byte lines (see RowPtr), so
+//     ldmatrix reads of 8 consecutive tokens hit distinct banks.  fp32: one
+//     bulk copy per token row, rows `row + 16` bytes apart.  Each sequence's
+//     query slice is copied once into a small ring of its own.
 //   * Warp w < Hg (a consumer) owns KV head w and its G query heads.  bf16:
 //     S^T[16 tok x 8] = K_tile[16 x D] * Q^T[D x 8] on the tensor cores
 //     (mma.sync m16n8k16, query heads padded to 8), online softmax in

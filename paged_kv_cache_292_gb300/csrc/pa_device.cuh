@@ -1,6 +1,7 @@
-// Device-side building blocks for sm_103a: mbarriers, bulk async copies
-// (the TMA engine's untiled form), ldmatrix / movmatrix and the bf16 tensor-core
-// MMA.  Inline PTX only; no library code.
+// Device-side building blocks for sm_103a: mbarriers, the TMA engine's bulk
+// (untiled) and tensor-map (tiled) async copies, ldmatrix / movmatrix, the
+// bf16 and f16 tensor-core MMAs and the E4M3 widening.  Inline PTX and CUDA
+// intrinsics only; no library code.
 #pragma once
 
 #include <cuda_bf16.h>
