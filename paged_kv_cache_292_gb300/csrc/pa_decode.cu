@@ -529,7 +529,9 @@ struct MmaConsumerMQ {
 //          output rows are permuted so that lane l/4 owns dims 2*(l/4) and
 //          +1 of each 16-wide slice, and one byte permute per register builds
 //          the (token, token) pairs the A operand needs.
-// Scores carry k_scale in scale_log2; v_scale is applied to the output.
+// Scores carry k_scale in scale_log2; v_scale is applied to the output.  The
+// bf16 query converts to f16 exactly for |q| in f16's normal range
+// [2^-14, 65504]; P enters as f16.
 template <int D>
 struct MmaConsumerF8 {
   static constexpr int KS = D / 16;
@@ -576,10 +578,8 @@ struct MmaConsumerF8 {
     for (int ks = 0; ks < KS; ++ks) {
       const uint32_t top = kr[ks >> 1][2 * (ks & 1)], bot = kr[ks >> 1][2 * (ks & 1) + 1];
       uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2(top);        // token row g: codes 0,1
-      a[1] = e4m3x2_to_f16x2(bot);        // token row g+8
-      a[2] = e4m3x2_to_f16x2(top >> 16);  // codes 2,3
-      a[3] = e4m3x2_to_f16x2(bot >> 16);
+      e4m3x4_to_f16x2x2(top, a[0], a[2]);  // token row g: codes 0,1 | codes 2,3
+      e4m3x4_to_f16x2x2(bot, a[1], a[3]);  // token row g+8
       if (ks & 1)
         mma_f16_16816(c1, a, qb[ks][0], qb[ks][1]);
       else
@@ -604,13 +604,13 @@ struct MmaConsumerF8 {
     m_b = mn_b;
     const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
     const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+    // Weights enter the f16 MMA rounded to f16 (relative error <= 2^-11,
+    // half an ulp of the 10-bit fraction), well inside the bf16 output's own
+    // rounding; the running sum keeps them in fp32.
     const uint32_t p_top = pack_f16x2(p0, p1), p_bot = pack_f16x2(p2, p3);
-    const uint32_t r_top = pack_f16x2(p0 - f16_lo(p_top), p1 - f16_hi(p_top));
-    const uint32_t r_bot = pack_f16x2(p2 - f16_lo(p_bot), p3 - f16_hi(p_bot));
     l_a = l_a * alpha_a + p0 + p2;
     l_b = l_b * alpha_b + p1 + p3;
     const uint32_t pb0 = movmatrix_trans(p_top), pb1 = movmatrix_trans(p_bot);
-    const uint32_t rb0 = movmatrix_trans(r_top), rb1 = movmatrix_trans(r_bot);
     // Each V register holds bytes (tok 2t: dim 2g, 2g+1 | tok 2t+1: dim 2g, 2g+1);
     // tokens past the end are zeroed (code 0 is +0.0) before they meet a weight.
     uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
@@ -618,21 +618,26 @@ struct MmaConsumerF8 {
       keep_lo = (t2 < nvalid ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid ? 0xffff0000u : 0u);
       keep_hi = (t2 + 8 < nvalid ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid ? 0xffff0000u : 0u);
     }
+    // Once the running maxima settle, most tiles leave every alpha at 1:
+    // skip the rescale then (this consumer is issue-bound).
+    if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        acc[mt][0] *= alpha_a;
+        acc[mt][1] *= alpha_b;
+        acc[mt][2] *= alpha_a;
+        acc[mt][3] *= alpha_b;
+      }
+    }
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       const uint32_t top = vr[mt >> 1][2 * (mt & 1)] & keep_lo;      // tokens 2t, 2t+1
       const uint32_t bot = vr[mt >> 1][2 * (mt & 1) + 1] & keep_hi;  // tokens 2t+8, 2t+9
+      // One byte permute per register: (dim 2g: tokens 2t, 2t+1 | dim 2g+1: same).
       uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2(__byte_perm(top, 0u, 0x0020));  // dim 2g: tokens 2t, 2t+1
-      a[1] = e4m3x2_to_f16x2(__byte_perm(top, 0u, 0x0031));  // dim 2g+1
-      a[2] = e4m3x2_to_f16x2(__byte_perm(bot, 0u, 0x0020));
-      a[3] = e4m3x2_to_f16x2(__byte_perm(bot, 0u, 0x0031));
-      acc[mt][0] *= alpha_a;
-      acc[mt][1] *= alpha_b;
-      acc[mt][2] *= alpha_a;
-      acc[mt][3] *= alpha_b;
+      e4m3x4_to_f16x2x2(__byte_perm(top, 0u, 0x3120), a[0], a[1]);
+      e4m3x4_to_f16x2x2(__byte_perm(bot, 0u, 0x3120), a[2], a[3]);
       mma_f16_16816(acc[mt], a, pb0, pb1);
-      mma_f16_16816(acc[mt], a, rb0, rb1);
     }
   }
 

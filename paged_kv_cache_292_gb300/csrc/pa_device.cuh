@@ -144,18 +144,16 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float f16_lo(uint32_t x) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xffffu)));
-}
-__device__ __forceinline__ float f16_hi(uint32_t x) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16)));
-}
-
-// Two E4M3 codes (low byte first) -> two f16 (low half first); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four E4M3 codes (byte 0 first) -> two f16x2 registers: `lo` holds codes
+// 0 and 1 (code 0 in its low half), `hi` codes 2 and 3.  Exact (every E4M3
+// value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
