@@ -39,7 +39,10 @@ from paged_kv_cache_292_gb300 import workloads  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_292_gb300", "csrc", "pa_decode.cu")
+# Sources the decode kernel is compiled from; their hash tags the committed
+# ncu traffic so that a changed kernel reports traffic null.
+KERNEL_SRCS = [os.path.join(ROOT, "paged_kv_cache_292_gb300", "csrc", f)
+               for f in ("pa_decode.cu", "pa_device.cuh", "pa_schedule.h", "pa_internal.h")]
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
@@ -79,17 +82,32 @@ def read_peaks():
 
 
 def kernel_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def read_traffic(workload: str):
+def traffic_key(workload: str, kv: str = "native", queries: int = 1, block_size=None) -> str:
+    """Key of one bench variant in profiles/traffic.json, e.g. "llama3_8b/fp8"."""
+    key = workload
+    if kv == "fp8":
+        key += "/fp8"
+    if queries > 1:
+        key += f"/q{queries}"
+    if block_size is not None:
+        key += f"/bs{block_size}"
+    return key
+
+
+def read_traffic(key: str):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
     or None if missing or taken on a different kernel source."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
-        rec = t.get(workload)
+        rec = t.get(key)
         if rec and rec.get("kernel_sha") == kernel_hash():
             return float(rec["dram_bytes_per_launch"])
     except Exception:
@@ -452,7 +470,7 @@ def run_ours(args):
 
     peak, peak_kind = read_peaks()
     achieved = by["decode"] / (dec_ms * 1e-3) / 1e9
-    traffic = read_traffic(args.workload)
+    traffic = read_traffic(traffic_key(args.workload, args.kv, args.queries, args.block_size))
     line = {
         "metric": "paged decode attention: effective KV GB/s (% of GB300 HBM peak), us/step",
         "value": value,
