@@ -361,13 +361,16 @@ struct MmaConsumerMQ {
   uint32_t qb[NT][KS][2];
   float acc[NT][KS][4];
   float m_a[NT], m_b[NT], l_a[NT], l_b[NT];
+  int col0 = 0;  // first (query, head) column this warp owns
 
+  // w: KV head within the CTA's group; col_base: first column of this warp.
   __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G, int Q,
-                                                int Hg, int lane) {
+                                                int Hg, int lane, int col_base) {
+    col0 = col_base;
     const int t2 = 2 * (lane & 3);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int n = nt * 8 + (lane >> 2);
+      const int n = col0 + nt * 8 + (lane >> 2);
       const bool real = n < G * Q;
       const int qi = real ? n / G : 0, g = real ? n % G : 0;
       const __nv_bfloat16* qh =
@@ -408,7 +411,7 @@ struct MmaConsumerMQ {
     float alpha_a[NT], alpha_b[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int na = nt * 8 + 2 * (lane & 3), nb = na + 1;
+      const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
       // Last visible position of each column's query (-1: padding column).
       const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
       const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
@@ -487,7 +490,7 @@ struct MmaConsumerMQ {
       }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const int n = nt * 8 + 2 * (lane & 3) + half;
+        const int n = col0 + nt * 8 + 2 * (lane & 3) + half;
         if (n >= G * Q) continue;
         const int qi = n / G, g = n % G;
         const int row = qi * H + kv_head * G + g;
@@ -832,16 +835,18 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 // (seq, kv_head).  Takes a ticket; the warp holding the last of the r1-r0+1
 // tickets merges every partial of that sequence and KV head by log-sum-exp,
 // writes the output rows, and resets the ticket counter.  Nobody waits.
+// `arrivals`: warps writing partials per range and KV head (two when the
+// (query, head) columns of a KV head are split across two warps).
 template <typename T, int D, bool kMQ>
 __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, int r0, int r1,
-                                 int slot0, int lane) {
+                                 int slot0, int lane, int arrivals = 1) {
   __threadfence();  // this warp's partial is visible before its ticket is
   __syncwarp();
   int* cnt = p.counters + (size_t)seq * p.num_kv_heads + kv_head;
   int ticket = 0;
   if (lane == 0) ticket = atomicAdd(cnt, 1);
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
-  if (ticket != r1 - r0) return;
+  if (ticket != arrivals * (r1 - r0 + 1) - 1) return;
   __threadfence();  // every other partial is visible now
   // Online pass over the partials, four query heads of this KV head at a
   // time: lane l owns dims [l*DL, l*DL+DL) of each head.  The next partial's
@@ -929,7 +934,8 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
 // Kernel 1
 // ---------------------------------------------------------------------------
 // QMODE 0: one query per sequence.  QMODE 1 / 2: several query tokens per
-// sequence with a causal mask, (query, head) columns in one / two MMA N-tiles.
+// sequence with a causal mask, (query, head) columns in one 8-wide MMA N-tile
+// per warp: one warp per KV head (up to 8 columns) or two (up to 16).
 template <typename T, int D, int GMAX, int QMODE, bool KV8 = false>
 __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     pa_decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -939,6 +945,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const int HG = p.num_head_groups, R = p.num_ranges, S = p.num_seqs;
   const int r = blockIdx.x / HG, hg = blockIdx.x % HG;
   const int Hg = p.heads_per_cta;
+  // QMODE 2 splits each KV head's 16 (query, head) columns over two warps.
+  constexpr int kSplit = QMODE == 2 ? 2 : 1;
+  const int NCW = Hg * kSplit;  // consumer warps; warp NCW is the producer
   constexpr bool kMmaPath = (sizeof(T) == 2);  // tensor-core consumers, swizzled stages
   const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes, kMmaPath);
   long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
@@ -994,11 +1003,11 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full_bar(i), 1);
-      mbar_init(empty_bar(i), Hg);
+      mbar_init(empty_bar(i), NCW);
     }
     for (int i = 0; i < NQ; ++i) {
       mbar_init(qfull_bar(i), 1);
-      mbar_init(qempty_bar(i), Hg);
+      mbar_init(qempty_bar(i), NCW);
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -1012,7 +1021,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       kMmaPath ? ((smem_addr(smem + L.stage) + 1023u) & ~1023u) : smem_addr(smem + L.stage);
   const int G = p.group, H = p.num_heads, Hk = p.num_kv_heads, bs = p.block_size;
 
-  if (warp == Hg) {
+  if (warp == NCW) {
     // ---------------- producer ----------------
     // Pool element: T, or one byte for an FP8 pool.
     using KV = typename std::conditional<KV8, unsigned char, T>::type;
@@ -1147,14 +1156,15 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     }
   } else {
     // ---------------- consumers ----------------
-    const int w = warp;
+    const int w = warp / kSplit;  // KV head within the group
+    const int col_base = (warp % kSplit) * 8;
     const int kv_head = hg * Hg + w;
     int st = 0, qi = 0;
     uint32_t ph = 0, qph = 0;
     constexpr bool kMma = (sizeof(T) == 2);
     using Mma = typename std::conditional<
         KV8, MmaConsumerF8<D>,
-        typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, (QMODE > 0 ? QMODE : 1)>>::type>::type;
+        typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, 1>>::type>::type;
     typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
     for (long long x = a; x < b; ++x) {
       if (!mbar_wait(full_bar(st), ph)) {
@@ -1170,7 +1180,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         if constexpr (QMODE == 0 || KV8)
           cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, lane);
         else
-          cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, p.num_queries, Hg, lane);
+          cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, p.num_queries, Hg, lane,
+                             col_base);
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty_bar(qi));
         if (++qi == NQ) {
@@ -1199,7 +1210,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         const int slot = ((mt.flags >> 2) & 3) - 1;
         cons.finish(p, mt.seq, kv_head, slot, r, lane);
         if (slot >= 0)
-          arrive_and_merge<T, D, (QMODE > 0)>(p, mt.seq, kv_head, mt.r0, mt.r1, (mt.flags >> 4) & 1, lane);
+          arrive_and_merge<T, D, (QMODE > 0)>(p, mt.seq, kv_head, mt.r0, mt.r1, (mt.flags >> 4) & 1, lane,
+                                              kSplit);
       }
       if (++st == NS) {
         st = 0;
@@ -1217,7 +1229,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
 namespace {
 
 struct Plan {
-  int Hg, HG, R, stages, q_slots;
+  int Hg, HG, R, stages, q_slots, split;
   uint32_t row_bytes, pitch, q_bytes, stage_bytes, smem;
   uint32_t lines, box_rows, box_bytes;  // tensor-core paths (see DecodeParams)
   size_t ws_ml, ws_o, ws_partials, ws_counters, ws_total;
@@ -1244,13 +1256,17 @@ size_t workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int head_
 }
 
 // KV heads one CTA stages per token row: the largest divisor of num_kv_heads
-// that is at most 8 (one consumer warp each) and keeps the row within 2 KiB,
-// so three stages fit in shared memory.
-int heads_per_cta(int num_kv_heads, int head_size, int elt) {
-  for (int h = kMaxGroupHeads; h > 1; --h)
+// that is at most `max_heads` (8 with one consumer warp per KV head, 4 with
+// two) and keeps the row within 2 KiB, so three stages fit in shared memory.
+int heads_per_cta(int num_kv_heads, int head_size, int elt, int max_heads = kMaxGroupHeads) {
+  for (int h = max_heads; h > 1; --h)
     if (num_kv_heads % h == 0 && h * head_size * elt <= kMaxRowBytes) return h;
   return 1;
 }
+
+// Consumer warps per KV head: two when a KV head has more than 8 (query, head)
+// columns (one 8-wide MMA tile per warp), else one.
+int column_split(int group, int num_queries) { return group * num_queries > 8 ? 2 : 1; }
 
 int default_ranges(const DeviceInfo& dev, int HG) {
   const int r = dev.sm_count / HG;
@@ -1274,7 +1290,8 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int 
   if (q_elt == 0) q_elt = elt;
   const int G = num_heads / num_kv_heads;
   const bool mma = q_elt == 2;
-  pl->Hg = heads_per_cta(num_kv_heads, head_size, elt);
+  pl->split = column_split(G, num_queries);
+  pl->Hg = heads_per_cta(num_kv_heads, head_size, elt, kMaxGroupHeads / pl->split);
   pl->HG = num_kv_heads / pl->Hg;
   pl->R = num_ranges > 0 ? num_ranges : default_ranges(dev, pl->HG);
   pl->row_bytes = (uint32_t)(pl->Hg * head_size * elt);
@@ -1434,7 +1451,8 @@ int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode smem)");
     configured[dev] = true;
   }
-  cudaError_t e = launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg + 1)), pl.smem, stream, prm);
+  cudaError_t e =
+      launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg * pl.split + 1)), pl.smem, stream, prm);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_decode_kernel");
   return PA_OK;
 }
@@ -1578,7 +1596,8 @@ size_t decode_workspace_size_q(int num_seqs, int num_heads, int num_kv_heads, in
     if (current_device_info(&dev) != PA_OK) return 0;
     // The head grouping depends on the element size; size for bf16, whose
     // larger groups leave more ranges per head group.
-    R = default_ranges(dev, num_kv_heads / heads_per_cta(num_kv_heads, head_size, 2));
+    const int split = column_split(num_heads / num_kv_heads, num_queries);
+    R = default_ranges(dev, num_kv_heads / heads_per_cta(num_kv_heads, head_size, 2, kMaxGroupHeads / split));
   }
   return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, R, nullptr, num_queries);
 }
