@@ -78,7 +78,8 @@ def test_range_split_variants_agree(name, num_ranges):
 EDGE_CTX = [1, 15, 16, 17, 31, 32, 33, 47, 48, 49, 0, 255, 256, 257, 2, 0]
 
 
-@pytest.mark.parametrize("block_size", [16, 32, 8, 1, 64])
+# Block sizes cover every tensor-copy box height gcd(bs, 16): 16, 8, 4 (12), 1 (1, 3).
+@pytest.mark.parametrize("block_size", [16, 32, 8, 1, 64, 3, 12, 24])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_edge_context_lengths(block_size, dtype):
     sp = workloads.spec("llama3_8b", dtype=dtype, num_seqs=len(EDGE_CTX), max_context=272, pool_blocks=0,

@@ -65,6 +65,12 @@ SMALL = {
     "long_split": workloads.spec("long_ctx", num_seqs=2, ctx_lo=3001, ctx_hi=3001, max_context=3008, pool_blocks=0),
     "gqa8_d64": workloads.spec("gqa8_70b", num_seqs=6, ctx_lo=1, ctx_hi=300, max_context=304, head_size=64),
     "gqa8_bs32": workloads.spec("gqa8_70b", num_seqs=6, ctx_lo=1, ctx_hi=300, max_context=320, block_size=32),
+    "llama_bs8": workloads.spec("llama3_8b", num_seqs=8, ctx_lo=1, ctx_hi=400, max_context=400, pool_blocks=0,
+                                block_size=8),
+    "llama_bs1": workloads.spec("llama3_8b", num_seqs=4, ctx_lo=1, ctx_hi=100, max_context=100, pool_blocks=0,
+                                block_size=1),
+    "llama_bs24": workloads.spec("llama3_8b", num_seqs=8, ctx_lo=1, ctx_hi=400, max_context=408, pool_blocks=0,
+                                 block_size=24),
 }
 
 

@@ -62,6 +62,30 @@ def test_multi_query_gqa8(Q, D):
     assert_close(out, _oracle(w, q), "bf16", f"G=8 Q={Q} D={D}")
 
 
+@pytest.mark.parametrize("Q", [2, 4])
+@pytest.mark.parametrize("block_size", [8, 1, 24])
+def test_multi_query_block_sizes(Q, block_size):
+    w, q = _case("llama3_8b", Q, **dict(SMALL_LLAMA, block_size=block_size, pool_blocks=0))
+    g = to_device(w)
+    out = binding.decode_multi(q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"], g["context_lens"], w.scale)
+    torch.cuda.synchronize()
+    assert_close(out, _oracle(w, q), "bf16", f"Q={Q} bs={block_size}")
+
+
+# More than 8 (query, head) columns per KV head: two warps per KV head, one of
+# them with padding columns when G * Q is not 16.
+@pytest.mark.parametrize("heads, kv_heads, Q", [(8, 1, 2), (12, 2, 2), (10, 2, 3), (32, 8, 3)])
+@pytest.mark.parametrize("num_ranges", [0, 1])
+def test_multi_query_split_columns(heads, kv_heads, Q, num_ranges):
+    w, q = _case("llama3_8b", Q, seed=heads, num_heads=heads, num_kv_heads=kv_heads, num_seqs=7, ctx_lo=1,
+                 ctx_hi=400, max_context=400, pool_blocks=0)
+    g = to_device(w)
+    out = binding.decode_multi(q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"], g["context_lens"], w.scale,
+                               num_ranges=num_ranges)
+    torch.cuda.synchronize()
+    assert_close(out, _oracle(w, q), "bf16", f"H={heads} Hk={kv_heads} Q={Q} R={num_ranges}")
+
+
 def test_short_contexts_give_zero_rows_for_queries_before_the_start():
     ctx = np.array([1, 2, 3, 4, 5, 17])
     sp = workloads.spec("llama3_8b", num_seqs=len(ctx), max_context=32, pool_blocks=0)
