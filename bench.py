@@ -239,6 +239,38 @@ def time_oracle(w, budget_s: float, max_seqs: int = None):
     return secs, nbytes, desc
 
 
+def unique_kv_bytes(w, e: int) -> int:
+    """K+V bytes of the distinct pool slots the batch reads (a shared prefix
+    counted once), beside the logical bytes that count it per sequence."""
+    bs = w.spec.block_size
+    seen = np.zeros(w.num_blocks * bs, dtype=bool)
+    bt, ctx = w.block_tables.numpy(), w.context_lens.numpy()
+    for s_, c in enumerate(ctx.tolist()):
+        n = -(-c // bs)
+        slots = (bt[s_, :n].astype(np.int64)[:, None] * bs + np.arange(bs)).reshape(-1)[:c]
+        seen[slots] = True
+    return int(seen.sum()) * 2 * w.spec.num_kv_heads * w.spec.head_size * e
+
+
+def oracle_single_thread(workload: str, budget_s: float):
+    """The oracle sample again in a child process with one BLAS/OpenMP thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", workload,
+                            "--cpu-budget", str(budget_s)], env=env, capture_output=True, text=True, timeout=300)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "sample": d["sample"]}
+    except Exception:
+        return None
+
+
+def run_oracle_sample(args):
+    w = make_replica(args.workload, 0, args.block_size)
+    secs, nbytes, desc = time_oracle(w, budget_s=args.cpu_budget)
+    print(json.dumps({"seconds": secs, "bytes": nbytes, "sample": desc}), flush=True)
+    return 0
+
+
 def cpu_threads() -> int:
     try:
         import threadpoolctl  # noqa: F401
@@ -419,8 +451,11 @@ def run_ours(args):
     # Timed region 2: the same K steps with events around each pa_decode call
     # on the launch stream, for the decode kernels' own duration (roofline).
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
+        wev[i][0].record(stream)
         write(g)
+        wev[i][1].record(stream)
         ev[i][0].record(stream)
         decode(g, out)
         ev[i][1].record(stream)
@@ -429,6 +464,7 @@ def run_ours(args):
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     dec_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    wr_ms = statistics.fmean(a.elapsed_time(b) for a, b in wev)
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_step = total_ms / args.steps
     value = job_throughput(by["step"], world, ms_step)
@@ -530,6 +566,8 @@ def run_ours(args):
             "num_seqs": S, "num_heads": H, "num_kv_heads": Hk, "head_size": D, "block_size": bs,
             "num_physical_blocks": NB, "context_tokens": int(w.context_lens.sum()),
             "step_bytes": by["step"], "decode_bytes": by["decode"], "write_bytes": by["write"],
+            "unique_kv_bytes": unique_kv_bytes(w, 1 if fp8 else (2 if sp.dtype == "bf16" else 4)),
+            "write_us": wr_ms * 1e3,
             "l2": f"inputs larger than L2: {by['kv_logical'] / 1e9:.3f} GB of K/V read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
             "replicas": world,
@@ -560,6 +598,10 @@ def run_ours(args):
         secs, nbytes, desc = time_oracle(w, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cpu_threads(),
                                 "kind": "oracle", "sample": desc, "seconds": secs}
+        if args.workload in ("tiny_fp32", "llama3_8b") and Q == 1 and not fp8 and args.block_size is None:
+            one = oracle_single_thread(args.workload, budget_s=min(5.0, args.cpu_budget))
+            if one is not None:
+                line["cpu_baseline"]["single_thread"] = one
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -570,8 +612,8 @@ def run_loop(args):
     """Steady-state decode driven by the host block manager, K steps.
 
     Each step: one batched pa_bm_append (one new token per sequence, blocks
-    allocated on demand), export of block tables and lengths into pinned host
-    buffers, their host-to-device copy, the cache write and the decode.  The
+    allocated on demand), export of block tables and lengths into a pinned
+    host buffer, its host-to-device copy, the cache write and the decode.  The
     timed region covers the host work too (wall clock, synchronised at both
     ends)."""
     from paged_kv_cache_292_gb300 import binding
@@ -601,22 +643,34 @@ def run_loop(args):
         bm.append(s_, c - 1)  # the prompt's K/V already sits in the (random) pool
     seqs = torch.arange(S, dtype=torch.int32)
     ones = torch.ones(S, dtype=torch.int32)
-    # Two sets of pinned host buffers, each reused only after the event that
-    # follows its host-to-device copies has completed: the host never
-    # overwrites a buffer an in-flight copy still reads.
-    bufs = [dict(slots=torch.empty(S, dtype=torch.int64).pin_memory(),
-                 tables=torch.empty((S, mb), dtype=torch.int32).pin_memory(),
-                 lens=torch.empty(S, dtype=torch.int32).pin_memory(),
-                 copied=torch.cuda.Event()) for _ in range(2)]
+    # Per step the manager's slots, tables and lengths go up in one copy from
+    # a packed pinned buffer.  Two buffer sets (host and device) alternate:
+    # the host refills set b only after its previous upload completed, and the
+    # upload into device set b waits until the kernels that last read it are
+    # done, so uploads run on their own stream beside the previous decode.
+    lay, total = {}, 0
+    for k, n, dt in (("slots", S, torch.int64), ("tables", S * mb, torch.int32), ("lens", S, torch.int32)):
+        lay[k] = (total, n, dt)
+        total += -(-n * torch.empty(0, dtype=dt).element_size() // 256) * 256
+
+    def carve(buf):
+        v = {k: buf[o:o + n * torch.empty(0, dtype=dt).element_size()].view(dt) for k, (o, n, dt) in lay.items()}
+        v["tables"] = v["tables"].view(S, mb)
+        return v
+
+    bufs = []
+    for _ in range(2):
+        hb = torch.empty(total, dtype=torch.uint8).pin_memory()
+        db = torch.empty(total, dtype=torch.uint8, device=dev)
+        bufs.append(dict(hbuf=hb, dbuf=db, h=carve(hb), d=carve(db), copied=torch.cuda.Event(),
+                         used=torch.cuda.Event()))
     copies_h = torch.empty(2 * S, dtype=torch.int32)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    slots_d = torch.empty(S, dtype=torch.int64, device=dev)
-    tables_d = torch.empty((S, mb), dtype=torch.int32, device=dev)
-    lens_d = torch.empty(S, dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
     ws_bytes = lib.pa_decode_workspace_size(S, H, Hk, D, 0)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    up = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
     P = binding._ptr
     nc, nd = ctypes.c_int(0), ctypes.c_int(0)
@@ -627,24 +681,27 @@ def run_loop(args):
         nonlocal host_s, it
         b = bufs[it % 2]
         it += 1
-        b["copied"].synchronize()  # the copy that last read these buffers is done
+        b["copied"].synchronize()  # the upload that last read this host set is done
         t0 = time.perf_counter()
-        rc = lib.pa_bm_append_batch(bm._h, S, P(seqs), P(ones), P(b["slots"]), P(copies_h), ctypes.addressof(nc),
+        h, d = b["h"], b["d"]
+        rc = lib.pa_bm_append_batch(bm._h, S, P(seqs), P(ones), P(h["slots"]), P(copies_h), ctypes.addressof(nc),
                                     ctypes.addressof(nd))
-        rc = rc or lib.pa_bm_export(bm._h, P(b["tables"]), P(b["lens"]))
+        rc = rc or lib.pa_bm_export(bm._h, P(h["tables"]), P(h["lens"]))
         host_s += time.perf_counter() - t0
         if rc:
             raise RuntimeError(binding.pa_last_error())
-        slots_d.copy_(b["slots"], non_blocking=True)
-        tables_d.copy_(b["tables"], non_blocking=True)
-        lens_d.copy_(b["lens"], non_blocking=True)
-        b["copied"].record(stream)
-        if lib.pa_write_cache(P(k_new), P(v_new), P(slots_d), P(k_cache), P(v_cache), S, Hk, D, bs, nb, sh,
+        up.wait_event(b["used"])  # the kernels that last read this device set are done
+        with torch.cuda.stream(up):
+            b["dbuf"].copy_(b["hbuf"], non_blocking=True)
+        b["copied"].record(up)
+        stream.wait_event(b["copied"])
+        if lib.pa_write_cache(P(k_new), P(v_new), P(d["slots"]), P(k_cache), P(v_cache), S, Hk, D, bs, nb, sh,
                               binding.dtype_code(tdt)):
             raise RuntimeError(binding.pa_last_error())
-        if lib.pa_decode_ex(P(out), P(q), P(k_cache), P(v_cache), P(tables_d), P(lens_d), S, H, Hk, D, bs, mb,
-                            1 / math.sqrt(D), sh, binding.dtype_code(tdt), nb, P(ws), ws_bytes, 0, P(err)):
+        if lib.pa_decode_ex(P(out), P(q), P(k_cache), P(v_cache), P(d["tables"]), P(d["lens"]), S, H, Hk, D, bs,
+                            mb, 1 / math.sqrt(D), sh, binding.dtype_code(tdt), nb, P(ws), ws_bytes, 0, P(err)):
             raise RuntimeError(binding.pa_last_error())
+        b["used"].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -697,11 +754,14 @@ def main():
                     help="query tokens per sequence (several: causal multi-query step via pa_decode_mq)")
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="KV pool element type: the workload's own, or E4M3 FP8 (quantising write + FP8 decode)")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--loop", action="store_true",
                     help="steady-state decode loop driven by the host block manager (separate metric)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.oracle_sample:
+        return run_oracle_sample(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.loop:
