@@ -27,9 +27,12 @@
  *   - context_lens[s] counts every valid token of sequence s, including the
  *     current step's (written by pa_write_cache first).  Token t of sequence s
  *     is row t % block_size of physical block block_tables[s][t / block_size].
- *     Table entries at or past ceil(context_lens[s] / block_size), and pool rows
- *     no valid token occupies, are never read.  context_lens[s] == 0 gives an
- *     all-zero output row.
+ *     Table entries at or past ceil(context_lens[s] / block_size) are never
+ *     read.  Pool rows no valid token occupies never affect the result; the
+ *     bf16 and FP8 decode paths do read the unused rows of a sequence's last,
+ *     partly filled block (they copy whole runs of rows), so those rows must
+ *     lie in the pool, but their contents (even NaN) do not matter.
+ *     context_lens[s] == 0 gives an all-zero output row.
  *   - Device-detected input faults (a block id outside [0, num_physical_blocks),
  *     a context length beyond max_blocks_per_seq * block_size or negative, a
  *     slot outside the pool) are reported by OR-ing PA_DEVERR_* bits into the
@@ -81,7 +84,11 @@ extern "C" {
  * context_lens [num_seqs] int32
  * Requirements: num_heads % num_kv_heads == 0 and num_heads / num_kv_heads <= 8;
  * head_size 64 or 128; block_size in [1, 4096]; query, out and both pools
- * 16-byte aligned.
+ * 16-byte aligned; for bf16, fewer than 2^31 token rows in the pool
+ * (num_physical_blocks * block_size) else PA_ERR_UNSUPPORTED.
+ * bf16 pools are read through TMA tensor maps built on the host for each call
+ * (cuTensorMapEncodeTiled, taken from the driver; PA_ERR_CUDA if the driver
+ * lacks it); block sizes that are multiples of 8 stream fastest.
  * The batch's tiles of 16 tokens are split into equal ranges, one CTA each.
  * A sequence cut by range boundaries leaves partial softmax statistics per
  * range; the last CTA to finish one of its KV heads merges them by
@@ -227,6 +234,9 @@ int pa_decode_static(void* out, const void* query, const void* k_cache, const vo
  * pa_decode_fp8 - pa_decode_ex over FP8 pools, query and out bf16: scores use
  * k = e4m3(code) * k_scale and values v = e4m3(code) * v_scale.  Each token
  * moves half the bytes of a bf16 pool.  Scratch as pa_decode_workspace_size.
+ * The query is rounded to f16 on the way into the tensor cores (exact for
+ * |q| in [2^-14, 65504]).  head_size 64 with an odd num_kv_heads is
+ * PA_ERR_UNSUPPORTED (a KV-head group's FP8 row must be whole 128-byte lines).
  */
 int pa_write_cache_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
                        void* k_cache, void* v_cache, int num_tokens, int num_kv_heads, int head_size,
