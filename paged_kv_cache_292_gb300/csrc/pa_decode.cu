@@ -840,14 +840,22 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 template <typename T, int D, bool kMQ>
 __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, int r0, int r1,
                                  int slot0, int lane, int arrivals = 1) {
-  __threadfence();  // this warp's partial is visible before its ticket is
-  __syncwarp();
+  // Release: the warp barrier orders every lane's partial stores before lane
+  // 0's fence, which makes them visible device-wide before the ticket.
+  // Acquire: the warp holding the last ticket fences before the barrier that
+  // releases its lanes to read the other partials.
+  const int last = arrivals * (r1 - r0 + 1) - 1;
   int* cnt = p.counters + (size_t)seq * p.num_kv_heads + kv_head;
+  __syncwarp();
   int ticket = 0;
-  if (lane == 0) ticket = atomicAdd(cnt, 1);
+  if (lane == 0) {
+    __threadfence();
+    ticket = atomicAdd(cnt, 1);
+    if (ticket == last) __threadfence();
+  }
+  __syncwarp();
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
-  if (ticket != arrivals * (r1 - r0 + 1) - 1) return;
-  __threadfence();  // every other partial is visible now
+  if (ticket != last) return;
   // Online pass over the partials, four query heads of this KV head at a
   // time: lane l owns dims [l*DL, l*DL+DL) of each head.  The next partial's
   // loads are issued before the current one is folded in.
