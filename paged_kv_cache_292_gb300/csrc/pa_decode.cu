@@ -541,6 +541,12 @@ struct MmaConsumerF8 {
   uint32_t qb[KS][2];
   float acc[KS][4];
   float m_a, m_b, l_a, l_b;
+  uint32_t lane_off = 0;  // this lane's ldmatrix row address within a half-stage (K and V alike)
+
+  // Once per kernel: uh is the head's first 16-byte unit in the group's row.
+  __device__ __forceinline__ void setup(uint32_t lines, int uh, int lane) {
+    lane_off = RowPtr<1>(0u, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines).a[0];
+  }
 
   __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G,
                                                 int lane) {
@@ -564,17 +570,18 @@ struct MmaConsumerF8 {
     l_a = l_b = 0.f;
   }
 
-  __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
-                                       int nvalid, float scale_log2, int lane) {
+  __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, int nvalid, float scale_log2,
+                                       int lane) {
     // Matrices of one ldmatrix.x4: (rows 0-7, bytes 0-15), (rows 8-15, 0-15),
     // (rows 0-7, 16-31), (rows 8-15, 16-31) - two k-steps / m-tiles of 16 dims.
-    const int r = (lane & 7) + ((lane >> 3) & 1) * 8, u0 = uh + (lane >> 4);
-    const RowPtr<1> kp(k_half, r, u0, lines), vp(v_half, r, u0, lines);
+    // Half-stages are 1 KiB aligned, so adding the lane offset keeps the
+    // swizzled unit bits that at(j)'s XOR steps through.
+    const uint32_t ka = k_half + lane_off, va = v_half + lane_off;
     uint32_t kr[KS / 2][4], vr[KS / 2][4];
 #pragma unroll
-    for (int j = 0; j < KS / 2; ++j) ldmatrix_x4(kr[j], kp.at(j));
+    for (int j = 0; j < KS / 2; ++j) ldmatrix_x4(kr[j], ka ^ ((uint32_t)(j & 3) << 5));
 #pragma unroll
-    for (int j = 0; j < KS / 2; ++j) ldmatrix_x4_trans(vr[j], vp.at(j));
+    for (int j = 0; j < KS / 2; ++j) ldmatrix_x4_trans(vr[j], va ^ ((uint32_t)(j & 3) << 5));
 
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -615,11 +622,18 @@ struct MmaConsumerF8 {
     l_b = l_b * alpha_b + p1 + p3;
     const uint32_t pb0 = movmatrix_trans(p_top), pb1 = movmatrix_trans(p_bot);
     // Each V register holds bytes (tok 2t: dim 2g, 2g+1 | tok 2t+1: dim 2g, 2g+1);
-    // tokens past the end are zeroed (code 0 is +0.0) before they meet a weight.
-    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+    // on the last tile of a segment, tokens past the end are zeroed (code 0
+    // is +0.0) before they meet a weight.
     if (nvalid < kTile) {
-      keep_lo = (t2 < nvalid ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid ? 0xffff0000u : 0u);
-      keep_hi = (t2 + 8 < nvalid ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid ? 0xffff0000u : 0u);
+      const uint32_t keep_lo = (t2 < nvalid ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid ? 0xffff0000u : 0u);
+      const uint32_t keep_hi = (t2 + 8 < nvalid ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int j = 0; j < KS / 2; ++j) {
+        vr[j][0] &= keep_lo;
+        vr[j][1] &= keep_hi;
+        vr[j][2] &= keep_lo;
+        vr[j][3] &= keep_hi;
+      }
     }
     // Once the running maxima settle, most tiles leave every alpha at 1:
     // skip the rescale then (this consumer is issue-bound).
@@ -634,8 +648,8 @@ struct MmaConsumerF8 {
     }
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
-      const uint32_t top = vr[mt >> 1][2 * (mt & 1)] & keep_lo;      // tokens 2t, 2t+1
-      const uint32_t bot = vr[mt >> 1][2 * (mt & 1) + 1] & keep_hi;  // tokens 2t+8, 2t+9
+      const uint32_t top = vr[mt >> 1][2 * (mt & 1)];      // tokens 2t, 2t+1
+      const uint32_t bot = vr[mt >> 1][2 * (mt & 1) + 1];  // tokens 2t+8, 2t+9
       // One byte permute per register: (dim 2g: tokens 2t, 2t+1 | dim 2g+1: same).
       uint32_t a[4];
       e4m3x4_to_f16x2x2(__byte_perm(top, 0u, 0x3120), a[0], a[1]);
@@ -1051,6 +1065,17 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       prefetch_tensormap(&p.tm_k);
       prefetch_tensormap(&p.tm_v);
     }
+    // Per-lane constants of the copy issue: whether this lane leads a copy
+    // (tensor paths: the first row of a box), where in a stage its copy
+    // lands, and which pool it reads.  Power-of-two block sizes take shifts
+    // and masks instead of integer division.
+    const bool lead = kMmaPath ? (t % (int)p.box_rows) == 0 : true;
+    const uint32_t lane_dst = kMmaPath ? (is_v ? kTile * p.lines * kLine : 0u) + t * p.lines * kLine
+                                       : (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
+    const void* tmap = is_v ? static_cast<const void*>(&p.tm_v) : static_cast<const void*>(&p.tm_k);
+    const int bs_sh = (bs & (bs - 1)) == 0 ? __ffs(bs) - 1 : -1;
+    auto blk_of = [&](int tok) { return bs_sh >= 0 ? tok >> bs_sh : tok / bs; };
+    auto off_of = [&](int tok) { return bs_sh >= 0 ? tok & (bs - 1) : tok % bs; };
     // Block-table window of the current sequence: lane i holds entry cb+i in
     // `cur` and cb+32+i in `nxt`.  The window slides one chunk at a time and the
     // next chunk is loaded a chunk ahead, so lookups never wait on memory except
@@ -1071,7 +1096,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const int j = static_cast<int>(x - ps);
       const int tok0 = j * kTile;
       const int nvalid = min(kTile, c - tok0);
-      const int blk0 = tok0 / bs;
+      const int blk0 = blk_of(tok0);
       if (new_seq) {
         slot = segment_slot(a, b, ps, ps + ns);
         if (slot >= 0) {
@@ -1120,10 +1145,10 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       // This lane's token -> physical block (a tile spans at most 16 blocks, so
       // it always lies inside the 64-entry window).
       const int tok = tok0 + t;
-      const int rel = tok / bs - cb;
+      const int rel = blk_of(tok) - cb;
       const int e_cur = __shfl_sync(0xffffffffu, cur, rel & 31);
       const int e_nxt = __shfl_sync(0xffffffffu, nxt, rel & 31);
-      long long phys = rel < 32 ? e_cur : e_nxt;
+      const int phys = rel < 32 ? e_cur : e_nxt;
       bool ok = t < nvalid;
       if (ok && p.num_physical_blocks > 0 && (phys < 0 || phys >= p.num_physical_blocks)) {
         report(p.error_flag, PA_DEVERR_BLOCK_ID);
@@ -1133,7 +1158,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       // t .. t + box_rows - 1, which lie in one block, as one tensor box; rows
       // past the context in that block come along and are masked by the
       // consumers.  fp32: one bulk copy per valid token row.
-      if constexpr (kMmaPath) ok = ok && (t % (int)p.box_rows) == 0;
+      ok = ok && lead;
       const unsigned copies = __ballot_sync(0xffffffffu, ok);
       if (!mbar_wait(empty_bar(st), ph ^ 1u)) {
         report(p.error_flag, PA_DEVERR_TIMEOUT);
@@ -1145,15 +1170,14 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       }
       __syncwarp();
       if (ok) {
+        const uint32_t dst = stages + st * p.stage_bytes + lane_dst;
+        // Token row of the pool: fewer than 2^31 in any pool that fits in device memory.
+        const int row = (int)((bs_sh >= 0 ? (unsigned)phys << bs_sh : (unsigned)phys * (unsigned)bs) +
+                              (unsigned)off_of(tok));
         if constexpr (kMmaPath) {
-          const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.lines * kLine : 0u) +
-                               t * p.lines * kLine;
-          tma_load_4d(dst, is_v ? &p.tm_v : &p.tm_k, 0, 0, hg, (int)(phys * bs + tok % bs),
-                      full_bar(st));
+          tma_load_4d(dst, tmap, 0, 0, hg, row, full_bar(st));
         } else {
-          const size_t row = ((size_t)phys * bs + tok % bs) * Hk + (size_t)hg * Hg;
-          const KV* src = (is_v ? vc : kc) + row * D;
-          const uint32_t dst = stages + st * p.stage_bytes + (is_v ? kTile * p.pitch : 0u) + t * p.pitch;
+          const KV* src = (is_v ? vc : kc) + ((size_t)row * Hk + (size_t)hg * Hg) * D;
           bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
         }
       }
@@ -1174,6 +1198,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         KV8, MmaConsumerF8<D>,
         typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, 1>>::type>::type;
     typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
+    if constexpr (KV8) cons.setup(p.lines, w * D / 16, lane);
     for (long long x = a; x < b; ++x) {
       if (!mbar_wait(full_bar(st), ph)) {
         report(p.error_flag, PA_DEVERR_TIMEOUT);
@@ -1202,7 +1227,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const uint32_t v_half = k_half + kTile * p.lines * kLine;
       const int uh = w * D * kKVBytes / 16;  // this head's first 16-byte unit in the row
       if constexpr (KV8) {
-        cons.tile(k_half, v_half, p.lines, uh, mt.nvalid, p.scale_log2, lane);
+        cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane);
       } else if constexpr (kMma && QMODE > 0) {
         cons.tile(k_half, v_half, p.lines, uh, mt.nvalid, mt.tok0, mt.ctx, G, p.num_queries,
                   p.scale_log2, lane);
