@@ -39,10 +39,10 @@ from paged_kv_cache_292_gb300 import workloads  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-# Sources the decode kernel is compiled from; their hash tags the committed
-# ncu traffic so that a changed kernel reports traffic null.
+# Sources the decode kernel's device code is compiled from; their hash tags
+# the committed ncu traffic so that a changed kernel reports traffic null.
 KERNEL_SRCS = [os.path.join(ROOT, "paged_kv_cache_292_gb300", "csrc", f)
-               for f in ("pa_decode.cu", "pa_device.cuh", "pa_schedule.h", "pa_internal.h")]
+               for f in ("pa_decode_kernel.cuh", "pa_device.cuh", "pa_schedule.h")]
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 

@@ -95,7 +95,10 @@ extern "C" {
  * log-sum-exp in a second pass over the partials.  The scratch for that comes
  * from a per-device buffer the library allocates (zero-filled) on first use
  * and grows when a larger batch needs it (cudaMalloc, which synchronises the
- * device; use pa_decode_ws to supply the scratch and never allocate).
+ * device; use pa_decode_ws to supply the scratch and never allocate).  That
+ * buffer is shared by every call on the device: calls that may run at the
+ * same time on different streams must use pa_decode_ws with scratch of their
+ * own.
  */
 int pa_decode(void* out, const void* query, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
