@@ -146,6 +146,27 @@ int pa_decode_ex(void* out, const void* query, const void* k_cache, const void* 
                  int32_t* error_flag);
 
 /*
+ * pa_decode_append - one decode step with its cache write fused in: for every
+ * sequence s with context_lens[s] >= 1, the K/V of its newest token (position
+ * context_lens[s] - 1) are k_new[s] / v_new[s]; the call stores them into the
+ * pool at that position (block_tables[s][(c-1) / block_size], row
+ * (c-1) % block_size) and returns the same `out` as pa_write_cache of those
+ * rows followed by pa_decode_ex.  One launch instead of two: the decode
+ * itself puts the new rows into its staged tile and into the pool.
+ * k_new, v_new  [num_seqs, num_kv_heads, head_size], 16-byte aligned
+ * The newest token's block must not be shared with another sequence of the
+ * batch (copy-on-write first, as pa_bm_append arranges).  dtype PA_BF16 only
+ * (PA_ERR_UNSUPPORTED otherwise).  Other arguments as in pa_decode_ex; a
+ * failed block-id check (num_physical_blocks > 0) leaves that token unwritten.
+ */
+int pa_decode_append(void* out, const void* query, const void* k_new, const void* v_new,
+                     void* k_cache, void* v_cache, const int32_t* block_tables,
+                     const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                     int head_size, int block_size, int max_blocks_per_seq, float scale,
+                     void* stream, int dtype, int num_physical_blocks, void* workspace,
+                     size_t workspace_bytes, int num_ranges, int32_t* error_flag);
+
+/*
  * pa_decode_mq - several query tokens per sequence over the paged cache, with
  * a causal mask: the chunked-prefill / speculative-decoding-verification step
  * (named by the vLLM book preface's reader questions and the is96 essay's

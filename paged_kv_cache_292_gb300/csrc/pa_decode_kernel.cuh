@@ -68,12 +68,18 @@ struct StageMeta {
   int flags;   // kSegBegin | kSegEnd | (output slot + 1) << 2 | (slot of range r0) << 4
   int r0, r1;  // first and last range touching the sequence (cut sequences only)
   int ctx;     // the sequence's context length (causal limits of several queries)
-  int pad1;
+  int newrow;  // appending calls: pool row of the sequence's newest token when this
+               // tile holds it (at tile row nvalid - 1); else -1
 };
 
 struct DecodeParams {
   CUtensorMap tm_k, tm_v;  // tensor-core paths: 4-D views of the pools (see make_tensor_maps)
   void* out;
+  // Appending calls (bf16, one query): K/V rows [num_seqs, num_kv_heads,
+  // head_size] of each sequence's newest token, written into the pool by the
+  // decode itself; nullptr otherwise.
+  const void* k_new;
+  const void* v_new;
   const void* q;
   const void* k_cache;
   const void* v_cache;
@@ -951,6 +957,37 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
   if (lane == 0) *cnt = 0;  // leave the counter zeroed for the next call
 }
 
+// Appending calls: the tile holding a sequence's newest token (row
+// mt.nvalid - 1) may have been staged before that token reached the pool, so
+// the warp of KV head kv_head puts the token's K and V (from k_new / v_new)
+// into its own columns of the staged rows, swizzled as the tensor copy lays
+// them out, and also stores them into the pool row for later steps.  Lane u
+// < 16 moves 16-byte unit u of the K row, lane 16 + u the same unit of V.
+template <int D>
+__device__ __forceinline__ void append_newest(const DecodeParams& p, const StageMeta& mt, int kv_head,
+                                              int w, uint32_t k_half, uint32_t v_half, int lane) {
+  constexpr int UH = D * 2 / 16;  // 16-byte units of one head's bf16 row
+  const int u = lane & 15;
+  const bool is_v = lane >= 16;
+  if (u < UH) {
+    const size_t e = ((size_t)mt.seq * p.num_kv_heads + kv_head) * D + u * 8;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+        static_cast<const __nv_bfloat16*>(is_v ? p.v_new : p.k_new) + e));
+    const uint32_t unit = (uint32_t)(w * UH + u);
+    const uint32_t L = (uint32_t)(mt.nvalid - 1) * p.lines + (unit >> 3);
+    const uint32_t dst = (is_v ? v_half : k_half) + L * kLine + (((unit & 7u) ^ (L & 7u)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val.x), "r"(val.y),
+                 "r"(val.z), "r"(val.w)
+                 : "memory");
+    __nv_bfloat16* pool = static_cast<__nv_bfloat16*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache));
+    *reinterpret_cast<uint4*>(pool + ((size_t)mt.newrow * p.num_kv_heads + kv_head) * D + u * 8) = val;
+  }
+  // The stage is later refilled by the TMA engine (async proxy): order these
+  // generic-proxy writes before that, and make them visible to the warp.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
 // ---------------------------------------------------------------------------
 // Kernel 1
 // ---------------------------------------------------------------------------
@@ -1163,16 +1200,27 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         report(p.error_flag, PA_DEVERR_TIMEOUT);
         break;
       }
+      // Token row of the pool: fewer than 2^31 in any pool that fits in device memory.
+      const int row = (int)((bs_sh >= 0 ? (unsigned)phys << bs_sh : (unsigned)phys * (unsigned)bs) +
+                            (unsigned)off_of(tok));
+      int newrow = -1;
+      if (kMmaPath && p.k_new != nullptr && tok0 + nvalid == c) {
+        // This tile holds the newest token (row nvalid - 1); a failed block
+        // check leaves it unwritten.
+        const int rn = __shfl_sync(0xffffffffu, row, nvalid - 1);
+        const int bad = __shfl_sync(0xffffffffu,
+                                    (int)(p.num_physical_blocks > 0 &&
+                                          (phys < 0 || phys >= p.num_physical_blocks)),
+                                    nvalid - 1);
+        newrow = bad ? -1 : rn;
+      }
       if (lane == 0) {
-        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, c, 0};
+        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, c, newrow};
         mbar_arrive_expect_tx(full_bar(st), __popc(copies) * (kMmaPath ? p.box_bytes : p.row_bytes));
       }
       __syncwarp();
       if (ok) {
         const uint32_t dst = stages + st * p.stage_bytes + lane_dst;
-        // Token row of the pool: fewer than 2^31 in any pool that fits in device memory.
-        const int row = (int)((bs_sh >= 0 ? (unsigned)phys << bs_sh : (unsigned)phys * (unsigned)bs) +
-                              (unsigned)off_of(tok));
         if constexpr (kMmaPath) {
           tma_load_4d(dst, tmap, 0, 0, hg, row, full_bar(st));
         } else {
@@ -1225,6 +1273,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const uint32_t k_half = stages + st * p.stage_bytes;
       const uint32_t v_half = k_half + kTile * p.lines * kLine;
       const int uh = w * D * kKVBytes / 16;  // this head's first 16-byte unit in the row
+      if constexpr (kMma && QMODE == 0 && !KV8) {
+        if (mt.newrow >= 0) append_newest<D>(p, mt, kv_head, w, k_half, v_half, lane);
+      }
       if constexpr (KV8) {
         cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane);
       } else if constexpr (kMma && QMODE > 0) {
