@@ -89,9 +89,12 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_key(workload: str, kv: str = "native", queries: int = 1, block_size=None) -> str:
+def traffic_key(workload: str, kv: str = "native", queries: int = 1, block_size=None,
+                separate: bool = False) -> str:
     """Key of one bench variant in profiles/traffic.json, e.g. "llama3_8b/fp8"."""
     key = workload
+    if separate:
+        key += "/separate"
     if kv == "fp8":
         key += "/fp8"
     if queries > 1:
@@ -388,7 +391,14 @@ def run_ours(args):
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # merge tickets start at zero
     P = binding._ptr
 
+    # The step: the newest tokens' cache write and the decode.  bf16 with one
+    # query per sequence runs both in one launch (pa_decode_append) unless
+    # --step separate asks for pa_write_cache + pa_decode.
+    fused = args.step == "fused" and not fp8 and Q == 1 and sp.dtype == "bf16"
+
     def write(gg, sh=sh):
+        if fused:
+            return
         if fp8:
             rc = lib.pa_write_cache_fp8(P(gg["k_new"]), P(gg["v_new"]), P(gg["slot_mapping"]), P(g["k_cache"]),
                                         P(g["v_cache"]), n_new, Hk, D, bs, NB, k_scale, v_scale, sh, dt, None)
@@ -399,7 +409,11 @@ def run_ours(args):
             raise RuntimeError(binding.pa_last_error())
 
     def decode(gg, o, sh=sh):
-        if fp8:
+        if fused:
+            rc = lib.pa_decode_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
+                                      P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, H, Hk, D,
+                                      bs, MB, w.scale, sh, dt, 0, P(ws), ws_bytes, 0, None)
+        elif fp8:
             rc = lib.pa_decode_fp8(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
                                    P(gg["context_lens"]), S, H, Hk, D, bs, MB, w.scale, k_scale, v_scale, sh, 0,
                                    P(ws), ws_bytes, 0, None)
@@ -544,8 +558,10 @@ def run_ours(args):
         return 0
 
     peak, peak_kind = read_peaks()
-    achieved = by["decode"] / (dec_ms * 1e-3) / 1e9
-    traffic = read_traffic(traffic_key(args.workload, args.kv, args.queries, args.block_size))
+    # A fused step's one launch also moves the cache write's bytes.
+    achieved = (by["step"] if fused else by["decode"]) / (dec_ms * 1e-3) / 1e9
+    traffic = read_traffic(traffic_key(args.workload, args.kv, args.queries, args.block_size,
+                                       separate=not fused and args.step == "separate"))
     line = {
         "metric": "paged decode attention: effective KV GB/s (% of GB300 HBM peak), us/step",
         "value": value,
@@ -567,7 +583,9 @@ def run_ours(args):
             "num_physical_blocks": NB, "context_tokens": int(w.context_lens.sum()),
             "step_bytes": by["step"], "decode_bytes": by["decode"], "write_bytes": by["write"],
             "unique_kv_bytes": unique_kv_bytes(w, 1 if fp8 else (2 if sp.dtype == "bf16" else 4)),
-            "write_us": wr_ms * 1e3,
+            "write_us": None if fused else wr_ms * 1e3,
+            "step": ("pa_decode_append (cache write fused into the decode, one launch)" if fused
+                     else "pa_write_cache + decode (two launches)"),
             "l2": f"inputs larger than L2: {by['kv_logical'] / 1e9:.3f} GB of K/V read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
             "replicas": world,
@@ -576,7 +594,9 @@ def run_ours(args):
             "launch": "CUDA graph replay" if args.graph else "eager (programmatic dependent launch)",
         },
         "roofline": {
-            "kernel": "pa_decode_kernel (one launch per pa_decode call; split sequences merged in-kernel)",
+            "kernel": ("pa_decode_kernel (one launch per step: cache write and decode; split sequences merged "
+                       "in-kernel)" if fused else
+                       "pa_decode_kernel (one launch per decode call; split sequences merged in-kernel)"),
             "bound": "hbm",
             "achieved": achieved,
             "peak": peak,
@@ -591,7 +611,7 @@ def run_ours(args):
                 "note": "per-step inputs (q, new K/V, slots, tables, lengths) uploaded from one pinned host "
                         "buffer and the output read back every step, double-buffered so transfers of adjacent "
                         "steps overlap the kernels; the paged pool is device-resident state"},
-        "gpu_launches": 2 * args.steps,  # write + decode per step (region 1)
+        "gpu_launches": (1 if fused else 2) * args.steps,  # launches per step in region 1
         "clocks": clk,
     }
     if args.cpu_baseline:
@@ -695,11 +715,18 @@ def run_loop(args):
             b["dbuf"].copy_(b["hbuf"], non_blocking=True)
         b["copied"].record(up)
         stream.wait_event(b["copied"])
-        if lib.pa_write_cache(P(k_new), P(v_new), P(d["slots"]), P(k_cache), P(v_cache), S, Hk, D, bs, nb, sh,
-                              binding.dtype_code(tdt)):
-            raise RuntimeError(binding.pa_last_error())
-        if lib.pa_decode_ex(P(out), P(q), P(k_cache), P(v_cache), P(d["tables"]), P(d["lens"]), S, H, Hk, D, bs,
-                            mb, 1 / math.sqrt(D), sh, binding.dtype_code(tdt), nb, P(ws), ws_bytes, 0, P(err)):
+        if tdt == torch.bfloat16 and args.step == "fused":
+            # The newest token sits at position len - 1, where the manager put its slot.
+            rc = lib.pa_decode_append(P(out), P(q), P(k_new), P(v_new), P(k_cache), P(v_cache), P(d["tables"]),
+                                      P(d["lens"]), S, H, Hk, D, bs, mb, 1 / math.sqrt(D), sh,
+                                      binding.dtype_code(tdt), nb, P(ws), ws_bytes, 0, P(err))
+        else:
+            rc = lib.pa_write_cache(P(k_new), P(v_new), P(d["slots"]), P(k_cache), P(v_cache), S, Hk, D, bs, nb,
+                                    sh, binding.dtype_code(tdt))
+            rc = rc or lib.pa_decode_ex(P(out), P(q), P(k_cache), P(v_cache), P(d["tables"]), P(d["lens"]), S, H,
+                                        Hk, D, bs, mb, 1 / math.sqrt(D), sh, binding.dtype_code(tdt), nb, P(ws),
+                                        ws_bytes, 0, P(err))
+        if rc:
             raise RuntimeError(binding.pa_last_error())
         b["used"].record(stream)
 
@@ -725,7 +752,9 @@ def run_loop(args):
         "warmup": args.warmup, "host_manager_us_per_step": host_s / steps * 1e6,
         "effective_kv_gbs": kv / (wall / steps) / 1e9, "n_gpus": 1, "dtype": sp.dtype, "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs": S, "block_size": bs, "num_physical_blocks": nb,
-                   "context_tokens_start": tokens0, "context_tokens_end": tokens1},
+                   "context_tokens_start": tokens0, "context_tokens_end": tokens1,
+                   "step": ("pa_decode_append (cache write fused into the decode)"
+                            if tdt == torch.bfloat16 and args.step == "fused" else "pa_write_cache + pa_decode_ex")},
     }
     print(json.dumps(line), flush=True)
     bm.close()
@@ -755,6 +784,9 @@ def main():
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="KV pool element type: the workload's own, or E4M3 FP8 (quantising write + FP8 decode)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--step", choices=["fused", "separate"], default="fused",
+                    help="bf16 one-query steps: cache write fused into the decode launch (default) or a "
+                         "separate pa_write_cache launch")
     ap.add_argument("--loop", action="store_true",
                     help="steady-state decode loop driven by the host block manager (separate metric)")
     args = ap.parse_args()
