@@ -156,7 +156,7 @@ int pa_decode_ex(void* out, const void* query, const void* k_cache, const void* 
  * k_new, v_new  [num_seqs, num_kv_heads, head_size], 16-byte aligned
  * The newest token's block must not be shared with another sequence of the
  * batch (copy-on-write first, as pa_bm_append arranges).  dtype PA_BF16 only
- * (PA_ERR_UNSUPPORTED otherwise).  Other arguments as in pa_decode_ex; a
+ * (PA_ERR_UNSUPPORTED otherwise; FP8 pools: pa_decode_fp8_append).  Other arguments as in pa_decode_ex; a
  * failed block-id check (num_physical_blocks > 0) leaves that token unwritten.
  */
 int pa_decode_append(void* out, const void* query, const void* k_new, const void* v_new,
@@ -272,6 +272,20 @@ int pa_decode_fp8(void* out, const void* query, const void* k_cache, const void*
                   int max_blocks_per_seq, float scale, float k_scale, float v_scale, void* stream,
                   int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
                   int32_t* error_flag);
+
+/*
+ * pa_decode_fp8_append - pa_decode_append over FP8 pools: the newest token's
+ * bf16 K/V (k_new/v_new [num_seqs, num_kv_heads, head_size]) are quantised
+ * as pa_write_cache_fp8 does (bit-identical codes) and written into the pools
+ * by the decode launch itself; out equals pa_write_cache_fp8 followed by
+ * pa_decode_fp8.  Scales, layouts and limits as in pa_decode_fp8.
+ */
+int pa_decode_fp8_append(void* out, const void* query, const void* k_new, const void* v_new,
+                         void* k_cache, void* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                         int head_size, int block_size, int max_blocks_per_seq, float scale,
+                         float k_scale, float v_scale, void* stream, int num_physical_blocks,
+                         void* workspace, size_t workspace_bytes, int num_ranges, int32_t* error_flag);
 
 /* Message for the calling thread's last non-zero return ("" if none). */
 const char* pa_last_error(void);

@@ -58,6 +58,11 @@ _SIGS = {
         _I,
         [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _I, _I, _P, _SZ, _I, _P],
     ),
+    "pa_decode_fp8_append": (
+        _I,
+        [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+         _P, _I, _P, _SZ, _I, _P],
+    ),
     "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "pa_decode_mq": (
         _I,
@@ -285,6 +290,24 @@ def decode_append(query, k_new, v_new, k_cache, v_cache, block_tables, context_l
     pa_decode_append(out, query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, S, H, Hk, D, bs,
                      block_tables.shape[1], float(scale), stream, dtype_code(query.dtype),
                      NB if check_block_ids else 0, workspace, ws_bytes, num_ranges, error_flag)
+    return out
+
+
+def decode_fp8_append(query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, k_scale,
+                      v_scale, out=None, stream=None, *, num_ranges=0, workspace=None, error_flag=None,
+                      check_block_ids=False):
+    """pa_decode_fp8_append: the FP8-pool step with the newest token's quantising write fused in."""
+    _require_cuda(query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, workspace, error_flag)
+    S, H, D = query.shape
+    NB, bs, Hk, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(query)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pa_decode_fp8_append(_ptr(out), _ptr(query), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                       _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), S, H, Hk, D, bs,
+                                       block_tables.shape[1], float(scale), float(k_scale), float(v_scale),
+                                       _stream(stream), NB if check_block_ids else 0, _ptr(workspace), ws_bytes,
+                                       num_ranges, _ptr(error_flag)))
     return out
 
 

@@ -284,8 +284,8 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   if (k_new != nullptr || v_new != nullptr) {
     if (k_new == nullptr || v_new == nullptr)
       return fail(PA_ERR_INVALID_ARG, "pa_decode_append: k_new and v_new are both needed");
-    if (dtype != PA_BF16 || kv_fp8 || num_queries != 1)
-      return fail(PA_ERR_UNSUPPORTED, "pa_decode_append: bf16 pools and one query per sequence only");
+    if (dtype != PA_BF16 || num_queries != 1)
+      return fail(PA_ERR_UNSUPPORTED, "pa_decode_append: bf16 queries and one query per sequence only");
     if (!aligned(k_new, 16) || !aligned(v_new, 16))
       return fail(PA_ERR_INVALID_ARG, "pa_decode_append: k_new / v_new not 16-byte aligned");
   }
@@ -367,6 +367,7 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   }
   prm.scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
   prm.v_scale = v_scale;
+  prm.k_scale = k_scale;
   prm.k_new = k_new;
   prm.v_new = v_new;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -465,6 +466,23 @@ extern "C" int pa_decode_append(void* out, const void* query, const void* k_new,
                            num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
                            stream, dtype, num_physical_blocks, workspace, workspace_bytes, num_ranges,
                            error_flag, false, 1.f, 1.f, k_new, v_new);
+}
+
+extern "C" int pa_decode_fp8_append(void* out, const void* query, const void* k_new, const void* v_new,
+                                    void* k_cache, void* v_cache, const int32_t* block_tables,
+                                    const int32_t* context_lens, int num_seqs, int num_heads,
+                                    int num_kv_heads, int head_size, int block_size,
+                                    int max_blocks_per_seq, float scale, float k_scale, float v_scale,
+                                    void* stream, int num_physical_blocks, void* workspace,
+                                    size_t workspace_bytes, int num_ranges, int32_t* error_flag) {
+  if (k_new == nullptr || v_new == nullptr) {
+    pa::clear_error();
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_fp8_append: null k_new / v_new");
+  }
+  return pa::decode_impl_q(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, 1,
+                           num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                           stream, PA_BF16, num_physical_blocks, workspace, workspace_bytes, num_ranges,
+                           error_flag, true, k_scale, v_scale, k_new, v_new);
 }
 
 extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,

@@ -97,6 +97,7 @@ struct DecodeParams {
   int stages, q_slots;
   int num_queries;  // query tokens per sequence (1 for plain decode)
   float v_scale;    // FP8 pools: value of a V code is decode(code) * v_scale (else 1)
+  float k_scale;    // FP8 pools: value of a K code is decode(code) * k_scale (else 1)
   uint32_t row_bytes, pitch, q_bytes, stage_bytes;
   uint32_t lines;      // tensor-core stages: 128-byte lines per staged token row
   uint32_t box_rows;   // token rows per tensor copy: gcd(block_size, 16)
@@ -988,6 +989,44 @@ __device__ __forceinline__ void append_newest(const DecodeParams& p, const Stage
   __syncwarp();
 }
 
+// The same for FP8 pools: the token's bf16 K/V are quantised exactly as the
+// FP8 cache write does (fp32 quotient by the pool's scale, E4M3 round to
+// nearest even, saturating), 16 codes per lane.
+template <int D>
+__device__ __forceinline__ void append_newest_fp8(const DecodeParams& p, const StageMeta& mt, int kv_head,
+                                                  int w, uint32_t k_half, uint32_t v_half, int lane) {
+  constexpr int UH = D / 16;  // 16-byte units of one head's FP8 row
+  const int u = lane & 15;
+  const bool is_v = lane >= 16;
+  if (u < UH) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(is_v ? p.v_new : p.k_new) +
+                                                      ((size_t)mt.seq * p.num_kv_heads + kv_head) * D + u * 16);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    const float sc = is_v ? p.v_scale : p.k_scale;
+    const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+          make_float2(bf16_lo(in[2 * i]) / sc, bf16_hi(in[2 * i]) / sc), __NV_SATFINITE, __NV_E4M3));
+      const uint32_t hi = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+          make_float2(bf16_lo(in[2 * i + 1]) / sc, bf16_hi(in[2 * i + 1]) / sc), __NV_SATFINITE, __NV_E4M3));
+      out[i] = lo | (hi << 16);
+    }
+    const uint32_t unit = (uint32_t)(w * UH + u);
+    const uint32_t L = (uint32_t)(mt.nvalid - 1) * p.lines + (unit >> 3);
+    const uint32_t dst = (is_v ? v_half : k_half) + L * kLine + (((unit & 7u) ^ (L & 7u)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(out[0]), "r"(out[1]), "r"(out[2]),
+                 "r"(out[3])
+                 : "memory");
+    unsigned char* pool = static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache));
+    *reinterpret_cast<uint4*>(pool + ((size_t)mt.newrow * p.num_kv_heads + kv_head) * D + u * 16) =
+        make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
 // ---------------------------------------------------------------------------
 // Kernel 1
 // ---------------------------------------------------------------------------
@@ -1273,8 +1312,13 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const uint32_t k_half = stages + st * p.stage_bytes;
       const uint32_t v_half = k_half + kTile * p.lines * kLine;
       const int uh = w * D * kKVBytes / 16;  // this head's first 16-byte unit in the row
-      if constexpr (kMma && QMODE == 0 && !KV8) {
-        if (mt.newrow >= 0) append_newest<D>(p, mt, kv_head, w, k_half, v_half, lane);
+      if constexpr (kMma && QMODE == 0) {
+        if (mt.newrow >= 0) {
+          if constexpr (KV8)
+            append_newest_fp8<D>(p, mt, kv_head, w, k_half, v_half, lane);
+          else
+            append_newest<D>(p, mt, kv_head, w, k_half, v_half, lane);
+        }
       }
       if constexpr (KV8) {
         cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane);

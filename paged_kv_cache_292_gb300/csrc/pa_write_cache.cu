@@ -220,18 +220,28 @@ extern "C" int pa_write_cache_fp8(const void* k_new, const void* v_new, const in
   if (num_tokens == 0) return PA_OK;
   const long long num_slots = (long long)num_physical_blocks * block_size;
   const int grid = num_tokens < 65535 ? num_tokens : 65535;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Programmatic dependent launch, as for pa_write_cache: the kernel may become
+  // resident while the one before it finishes and waits for it in-kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (src_dtype == PA_BF16)
-    pa::pa_write_cache_fp8_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), slot_mapping,
-        static_cast<uint32_t*>(k_cache), static_cast<uint32_t*>(v_cache), num_tokens, (int)row_elems,
-        num_slots, k_scale, v_scale, error_flag);
+    e = cudaLaunchKernelEx(&cfg, pa::pa_write_cache_fp8_kernel<__nv_bfloat16>,
+                           static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+                           slot_mapping, static_cast<uint32_t*>(k_cache), static_cast<uint32_t*>(v_cache),
+                           num_tokens, (int)row_elems, num_slots, k_scale, v_scale, error_flag);
   else
-    pa::pa_write_cache_fp8_kernel<float><<<grid, 128, 0, st>>>(
-        static_cast<const float*>(k_new), static_cast<const float*>(v_new), slot_mapping,
-        static_cast<uint32_t*>(k_cache), static_cast<uint32_t*>(v_cache), num_tokens, (int)row_elems,
-        num_slots, k_scale, v_scale, error_flag);
-  const cudaError_t e = cudaGetLastError();
+    e = cudaLaunchKernelEx(&cfg, pa::pa_write_cache_fp8_kernel<float>, static_cast<const float*>(k_new),
+                           static_cast<const float*>(v_new), slot_mapping, static_cast<uint32_t*>(k_cache),
+                           static_cast<uint32_t*>(v_cache), num_tokens, (int)row_elems, num_slots, k_scale,
+                           v_scale, error_flag);
   if (e != cudaSuccess) return pa::cuda_fail(e, "launch pa_write_cache_fp8_kernel");
   return PA_OK;
 }

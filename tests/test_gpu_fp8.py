@@ -113,3 +113,32 @@ def test_fp8_write_then_decode_step():
     want = ofp8.decode_fp8(w.q.double().numpy(), k_ref, v_ref, w.block_tables.numpy(), w.context_lens.numpy(),
                            w.scale, bs, k_scale, v_scale)
     assert_close(out, want, "bf16", "fp8 step")
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "long_split", "gqa8_d64", "llama_bs8", "llama_bs1", "llama_bs24"])
+@pytest.mark.parametrize("num_ranges", [0, 997])
+def test_fp8_append_equals_write_then_decode(name, num_ranges):
+    """pa_decode_fp8_append: the newest tokens' quantising write fused into the
+    decode gives the pools and output of pa_write_cache_fp8 + pa_decode_fp8."""
+    sp = SMALL[name]
+    w = workloads.make_workload(sp, prewritten=False)
+    k_scale, v_scale = 0.37, 2.5
+    kcode = _codes_of_pool(w, w.k_cache, k_scale)
+    vcode = _codes_of_pool(w, w.v_cache, v_scale)
+    bs = sp.block_size
+    for s, c in enumerate(w.context_lens.tolist()):  # the newest slot holds poison until written
+        if c > 0:
+            slot = int(w.slot_mapping[s])
+            kcode[slot // bs, slot % bs] = NAN_CODE
+            vcode[slot // bs, slot % bs] = NAN_CODE
+    q, kn, vn = w.q.cuda(), w.k_new.cuda(), w.v_new.cuda()
+    bt, cl = w.block_tables.cuda(), w.context_lens.cuda()
+    ka, va = torch.from_numpy(kcode).cuda(), torch.from_numpy(vcode).cuda()
+    binding.write_cache_fp8(kn, vn, w.slot_mapping.cuda(), ka, va, k_scale, v_scale)
+    out_a = binding.decode_fp8(q, ka, va, bt, cl, w.scale, k_scale, v_scale, num_ranges=num_ranges)
+    kb, vb = torch.from_numpy(kcode).cuda(), torch.from_numpy(vcode).cuda()
+    out_b = binding.decode_fp8_append(q, kn, vn, kb, vb, bt, cl, w.scale, k_scale, v_scale, num_ranges=num_ranges,
+                                      check_block_ids=True)
+    torch.cuda.synchronize()
+    assert torch.equal(kb, ka) and torch.equal(vb, va)
+    assert torch.equal(out_b.view(torch.int16), out_a.view(torch.int16))
