@@ -394,7 +394,7 @@ def run_ours(args):
     # The step: the newest tokens' cache write and the decode.  bf16 with one
     # query per sequence runs both in one launch (pa_decode_append) unless
     # --step separate asks for pa_write_cache + pa_decode.
-    fused = args.step == "fused" and not fp8 and Q == 1 and sp.dtype == "bf16"
+    fused = args.step == "fused" and Q == 1 and sp.dtype == "bf16"
 
     def write(gg, sh=sh):
         if fused:
@@ -409,7 +409,11 @@ def run_ours(args):
             raise RuntimeError(binding.pa_last_error())
 
     def decode(gg, o, sh=sh):
-        if fused:
+        if fused and fp8:
+            rc = lib.pa_decode_fp8_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
+                                          P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, H, Hk, D,
+                                          bs, MB, w.scale, k_scale, v_scale, sh, 0, P(ws), ws_bytes, 0, None)
+        elif fused:
             rc = lib.pa_decode_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
                                       P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, H, Hk, D,
                                       bs, MB, w.scale, sh, dt, 0, P(ws), ws_bytes, 0, None)
@@ -590,8 +594,9 @@ def run_ours(args):
             "step_bytes": by["step"], "decode_bytes": by["decode"], "write_bytes": by["write"],
             "unique_kv_bytes": unique_kv_bytes(w, 1 if fp8 else (2 if sp.dtype == "bf16" else 4)),
             "write_us": None if fused else wr_ms * 1e3,
-            "step": ("pa_decode_append (cache write fused into the decode, one launch)" if fused
-                     else "pa_write_cache + decode (two launches)"),
+            "step": (("pa_decode_fp8_append" if fp8 else "pa_decode_append") +
+                     " (cache write fused into the decode, one launch)" if fused
+                     else "cache write + decode (two launches)"),
             "l2": f"inputs larger than L2: {by['kv_logical'] / 1e9:.3f} GB of K/V read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
             "replicas": world,
@@ -794,8 +799,8 @@ def main():
                     help="KV pool element type: the workload's own, or E4M3 FP8 (quantising write + FP8 decode)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--step", choices=["fused", "separate"], default="fused",
-                    help="bf16 one-query steps: cache write fused into the decode launch (default) or a "
-                         "separate pa_write_cache launch")
+                    help="one-query bf16/FP8 steps: cache write fused into the decode launch (default) or a "
+                         "separate cache-write launch")
     ap.add_argument("--loop", action="store_true",
                     help="steady-state decode loop driven by the host block manager (separate metric)")
     args = ap.parse_args()
