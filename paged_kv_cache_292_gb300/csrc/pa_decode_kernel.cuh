@@ -7,15 +7,15 @@
 // attend with the step's query (step 4) and write the output (step 5).  The
 // same section's "精妙之处" asks for the gather to be planned up front and for
 // copies to overlap compute on the GPU's separate copy engine; here that is a
-// producer warp driving the TMA engine's bulk copies into a ring of shared-
-// memory stages while consumer warps compute on earlier stages.
+// producer warp driving the TMA engine's copies into a ring of shared-memory
+// stages while consumer warps compute on earlier stages.
 //
 // Kernel 1 (pa_decode_kernel), one CTA per (token range, KV-head group):
 //   * The flattened tile list of the batch is cut into equal ranges (see
 //     pa_schedule.h), so every CTA moves the same K/V bytes.
-//   * Warp `Hg` (the producer) walks the range tile by tile.  For each tile of
+//   * The last warp (the producer) walks the range tile by tile.  For each tile of
 //     16 tokens it looks up the block ids and copies K and V into the stage.
-//     A token row is all `Hg` KV heads of the token, contiguous in the pool
+//     A token row is the `Hg` KV heads of the CTA's group, contiguous in the pool
 //     ([block, slot, head, dim] layout), e.g. 2 KiB for 8 heads x 128 x bf16.
 //     Tensor-core paths (bf16, FP8): one tensor-map box per run of
 //     gcd(block_size, 16) rows of one block, landing with the 128-byte
@@ -23,12 +23,16 @@
 //     ldmatrix reads of 8 consecutive tokens hit distinct banks.  fp32: one
 //     bulk copy per token row, rows `row + 16` bytes apart.  Each sequence's
 //     query slice is copied once into a small ring of its own.
-//   * Warp w < Hg (a consumer) owns KV head w and its G query heads.  bf16:
-//     S^T[16 tok x 8] = K_tile[16 x D] * Q^T[D x 8] on the tensor cores
-//     (mma.sync m16n8k16, query heads padded to 8), online softmax in
-//     registers (running max and sum in the exp2 domain), then
-//     O^T[D x 8] += V^T[D x 16] * P^T[16 x 8], with P^T obtained from the score
-//     fragment by movmatrix.  fp32: the same on CUDA cores.
+//   * Each consumer warp owns one KV head and its G query heads (with several
+//     query tokens and more than 8 (query, head) columns, two warps share a KV
+//     head, 8 columns each).  bf16: S^T[16 tok x 8] = K_tile[16 x D] *
+//     Q^T[D x 8] on the tensor cores (mma.sync m16n8k16, query heads padded
+//     to 8), online softmax in registers (running max and sum in the exp2
+//     domain), then O^T[D x 8] += V^T[D x 16] * P^T[16 x 8], with P^T obtained
+//     from the score fragment by movmatrix.  FP8 pools: codes widened to f16
+//     (MmaConsumerF8).  fp32: the same on CUDA cores.
+//   * Appending calls also write each sequence's newest token: the consumer
+//     warps put it into the staged tile and into the pool (append_newest).
 //   * A sequence wholly inside the range is written to `out` directly.  A
 //     sequence cut by range boundaries leaves one (m, l, O) partial per range
 //     and KV head; the warp that writes the last of them (an atomic ticket per
