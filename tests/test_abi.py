@@ -92,6 +92,43 @@ def test_write_cache_rejects_bad_arguments_on_host(lib, kw, code):
     assert rc == code
 
 
+@pytest.mark.parametrize(
+    "kw, code",
+    [
+        (dict(k_new=None), binding.PA_ERR_INVALID_ARG),
+        (dict(v_new=None), binding.PA_ERR_INVALID_ARG),
+        (dict(k_new=24), binding.PA_ERR_INVALID_ARG),  # misaligned
+        (dict(dtype=binding.PA_F32), binding.PA_ERR_UNSUPPORTED),
+        (dict(block_tables=None), binding.PA_ERR_INVALID_ARG),
+    ],
+)
+def test_decode_append_rejects_bad_arguments_on_host(lib, kw, code):
+    a = dict(out=16, query=16, k_new=16, v_new=16, k_cache=16, v_cache=16, block_tables=16, context_lens=16,
+             dtype=binding.PA_BF16)
+    a.update(kw)
+    rc = lib.pa_decode_append(a["out"], a["query"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"],
+                              a["block_tables"], a["context_lens"], 1, 8, 8, 128, 16, 4, 0.1, 0, a["dtype"], 0,
+                              None, 0, 0, None)
+    assert rc == code
+    assert lib.pa_last_error().decode()
+
+
+@pytest.mark.parametrize(
+    "kw, code",
+    [
+        (dict(k_new=None), binding.PA_ERR_INVALID_ARG),
+        (dict(k_scale=0.0), binding.PA_ERR_INVALID_ARG),
+        (dict(v_scale=float("inf")), binding.PA_ERR_INVALID_ARG),
+    ],
+)
+def test_decode_fp8_append_rejects_bad_arguments_on_host(lib, kw, code):
+    a = dict(k_new=16, k_scale=1.0, v_scale=1.0)
+    a.update(kw)
+    rc = lib.pa_decode_fp8_append(16, 16, a["k_new"], 16, 16, 16, 16, 16, 1, 8, 8, 128, 16, 4, 0.1, a["k_scale"],
+                                  a["v_scale"], 0, 0, None, 0, 0, None)
+    assert rc == code
+
+
 def test_workspace_size_formula(lib):
     def up(x):
         return (x + 255) // 256 * 256
