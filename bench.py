@@ -401,10 +401,14 @@ def run_ours(args):
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)  # merge tickets start at zero
     P = binding._ptr
 
-    # The step: the newest tokens' cache write and the decode.  bf16 with one
-    # query per sequence runs both in one launch (pa_decode_append) unless
-    # --step separate asks for pa_write_cache + pa_decode.
-    fused = args.step == "fused" and Q == 1 and sp.dtype == "bf16"
+    # The step: the newest tokens' cache write and the decode.  bf16 queries
+    # run both in one launch (pa_decode_append, pa_decode_fp8_append or, with
+    # several queries per sequence, pa_decode_mq_append) unless --step
+    # separate asks for the cache write and the decode as two launches.
+    fused = args.step == "fused" and sp.dtype == "bf16"
+    # With more than 8 (query, head) columns per KV head the appending call
+    # writes the rows with its own kernel ahead of the decode: two launches.
+    launches = 1 if fused and (H // Hk) * Q <= 8 else 2
 
     def write(gg, sh=sh):
         if fused:
@@ -423,6 +427,10 @@ def run_ours(args):
             rc = lib.pa_decode_fp8_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
                                           P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, H, Hk, D,
                                           bs, MB, w.scale, k_scale, v_scale, sh, 0, P(ws), ws_bytes, 0, None)
+        elif fused and Q > 1:
+            rc = lib.pa_decode_mq_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
+                                         P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, Q, H, Hk,
+                                         D, bs, MB, w.scale, sh, dt, 0, P(ws), ws_bytes, 0, None)
         elif fused:
             rc = lib.pa_decode_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
                                       P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, H, Hk, D,
@@ -604,8 +612,9 @@ def run_ours(args):
             "step_bytes": by["step"], "decode_bytes": by["decode"], "write_bytes": by["write"],
             "unique_kv_bytes": unique_kv_bytes(w, 1 if fp8 else (2 if sp.dtype == "bf16" else 4)),
             "write_us": None if fused else wr_ms * 1e3,
-            "step": (("pa_decode_fp8_append" if fp8 else "pa_decode_append") +
-                     " (cache write fused into the decode, one launch)" if fused
+            "step": (("pa_decode_fp8_append" if fp8 else "pa_decode_mq_append" if Q > 1 else "pa_decode_append") +
+                     (" (cache write fused into the decode, one launch)" if launches == 1
+                      else " (row-writing kernel chained ahead of the decode, two launches)") if fused
                      else "cache write + decode (two launches)"),
             "l2": f"inputs larger than L2: {by['kv_logical'] / 1e9:.3f} GB of K/V read per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
@@ -616,7 +625,8 @@ def run_ours(args):
         },
         "roofline": {
             "kernel": ("pa_decode_kernel (one launch per step: cache write and decode; split sequences merged "
-                       "in-kernel)" if fused else
+                       "in-kernel)" if launches == 1 else
+                       "pa_append_rows_kernel + pa_decode_kernel (step bytes over the step time)" if fused else
                        "pa_decode_kernel (one launch per decode call; split sequences merged in-kernel)"),
             "bound": "hbm",
             "achieved": achieved,
@@ -627,7 +637,7 @@ def run_ours(args):
             "traffic": traffic,
             "decode_us": kern_ms * 1e3,
             "decode_us_per_call_events": dec_ms * 1e3,
-            "timing": ("region 1: back-to-back launches, one per step" if fused
+            "timing": (f"region 1: back-to-back steps, {launches} launch(es) each" if fused
                        else "region 2: events around each decode call"),
         },
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -635,7 +645,7 @@ def run_ours(args):
                 "note": "per-step inputs (q, new K/V, slots, tables, lengths) uploaded from one pinned host "
                         "buffer and the output read back every step, double-buffered so transfers of adjacent "
                         "steps overlap the kernels; the paged pool is device-resident state"},
-        "gpu_launches": (1 if fused else 2) * args.steps,  # launches per step in region 1
+        "gpu_launches": launches * args.steps,  # launches per step in region 1
         "clocks": clk,
     }
     if args.cpu_baseline:

@@ -196,6 +196,32 @@ size_t pa_decode_mq_workspace_size(int num_seqs, int num_queries, int num_heads,
                                    int head_size, int num_ranges);
 
 /*
+ * pa_decode_mq_append - pa_decode_mq with the step's cache write fused in: for
+ * every sequence s with context c = context_lens[s], the K/V of its query
+ * token i (position c - num_queries + i) are k_new[s * num_queries + i] /
+ * v_new[s * num_queries + i]; the call stores each token whose position is
+ * >= 0 into the pool (block_tables[s][pos / block_size], row
+ * pos % block_size) and returns the same `out` as pa_write_cache of those
+ * rows followed by pa_decode_mq.  One launch instead of two when
+ * (num_heads / num_kv_heads) * num_queries <= 8; above that (two consumer
+ * warps per KV head) the call launches a row-writing kernel and then the
+ * decode on `stream`, chained by programmatic dependent launch.
+ * k_new, v_new  [num_seqs * num_queries, num_kv_heads, head_size], bf16,
+ *               16-byte aligned
+ * The blocks of the new tokens must not be shared with another sequence of
+ * the batch.  dtype PA_BF16 only (PA_ERR_UNSUPPORTED otherwise).  Other
+ * arguments, scratch size and limits as in pa_decode_mq; a failed block-id
+ * check (num_physical_blocks > 0) leaves that token unwritten.
+ */
+int pa_decode_mq_append(void* out, const void* query, const void* k_new, const void* v_new,
+                        void* k_cache, void* v_cache, const int32_t* block_tables,
+                        const int32_t* context_lens, int num_seqs, int num_queries, int num_heads,
+                        int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
+                        float scale, void* stream, int dtype, int num_physical_blocks,
+                        void* workspace, size_t workspace_bytes, int num_ranges,
+                        int32_t* error_flag);
+
+/*
  * pa_write_cache - scatter one step's new K/V rows into the paged pool
  * (the "reshape_and_cache" step).  For every token i with slot_mapping[i] >= 0:
  *   k_cache[slot / block_size, slot % block_size, :, :] = k_new[i, :, :]  (bit copy)

@@ -69,6 +69,11 @@ _SIGS = {
         [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _I, _I, _P, _SZ, _I, _P],
     ),
     "pa_decode_mq_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "pa_decode_mq_append": (
+        _I,
+        [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _I, _I, _P, _SZ, _I,
+         _P],
+    ),
     "pa_write_cache_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, ctypes.c_float, _P, _I, _P]),
     "pa_decode_fp8": (
         _I,
@@ -290,6 +295,35 @@ def decode_append(query, k_new, v_new, k_cache, v_cache, block_tables, context_l
     pa_decode_append(out, query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, S, H, Hk, D, bs,
                      block_tables.shape[1], float(scale), stream, dtype_code(query.dtype),
                      NB if check_block_ids else 0, workspace, ws_bytes, num_ranges, error_flag)
+    return out
+
+
+def pa_decode_mq_append(out, query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                        num_queries, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                        stream=None, dtype=None, num_physical_blocks=0, workspace=None, workspace_bytes=0,
+                        num_ranges=0, error_flag=None):
+    dtype = dtype_code(query.dtype) if dtype is None else dtype
+    _check(load().pa_decode_mq_append(_ptr(out), _ptr(query), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), num_seqs, num_queries,
+                                      num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq,
+                                      float(scale), _stream(stream), dtype, num_physical_blocks, _ptr(workspace),
+                                      workspace_bytes, num_ranges, _ptr(error_flag)))
+
+
+def decode_multi_append(query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                        stream=None, *, num_ranges=0, workspace=None, error_flag=None, check_block_ids=False):
+    """Several causal query tokens per sequence with their K/V (k_new/v_new[S*Q, Hk, D], token i of
+    sequence s at row s*Q+i, position context_lens[s]-Q+i) written into the pools by the same launch
+    (shapes as in ``pa_decode_mq_append``)."""
+    _require_cuda(query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, workspace, error_flag)
+    S, Q, H, D = query.shape
+    NB, bs, Hk, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(query)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    pa_decode_mq_append(out, query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, S, Q, H, Hk, D,
+                        bs, block_tables.shape[1], float(scale), stream, dtype_code(query.dtype),
+                        NB if check_block_ids else 0, workspace, ws_bytes, num_ranges, error_flag)
     return out
 
 

@@ -284,8 +284,9 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   if (k_new != nullptr || v_new != nullptr) {
     if (k_new == nullptr || v_new == nullptr)
       return fail(PA_ERR_INVALID_ARG, "pa_decode_append: k_new and v_new are both needed");
-    if (dtype != PA_BF16 || num_queries != 1)
-      return fail(PA_ERR_UNSUPPORTED, "pa_decode_append: bf16 queries and one query per sequence only");
+    if (dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_decode_append: bf16 queries and pools only");
+    if (kv_fp8 && num_queries != 1)
+      return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8_append: one query per sequence");
     if (!aligned(k_new, 16) || !aligned(v_new, 16))
       return fail(PA_ERR_INVALID_ARG, "pa_decode_append: k_new / v_new not 16-byte aligned");
   }
@@ -371,6 +372,15 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   prm.k_new = k_new;
   prm.v_new = v_new;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (k_new != nullptr && pl.split == 2) {
+    // Two consumer warps per KV head: the rows are written by their own
+    // kernel, chained ahead of the decode, which then only reads them.
+    rc = append_rows_impl(k_new, v_new, block_tables, context_lens, const_cast<void*>(k_cache),
+                          const_cast<void*>(v_cache), num_seqs, num_queries, num_kv_heads, head_size,
+                          block_size, max_blocks_per_seq, num_physical_blocks, stream, error_flag);
+    if (rc != PA_OK) return rc;
+    prm.k_new = prm.v_new = nullptr;
+  }
   if (dtype == PA_BF16) {
     return head_size == 64 ? launch_dtype<__nv_bfloat16, 64>(prm, pl, dev.device, st, kv_fp8)
                            : launch_dtype<__nv_bfloat16, 128>(prm, pl, dev.device, st, kv_fp8);
@@ -500,6 +510,23 @@ extern "C" int pa_decode_mq(void* out, const void* query, const void* k_cache, c
                            num_queries, num_heads, num_kv_heads, head_size, block_size,
                            max_blocks_per_seq, scale, stream, dtype, num_physical_blocks, workspace,
                            workspace_bytes, num_ranges, error_flag);
+}
+
+extern "C" int pa_decode_mq_append(void* out, const void* query, const void* k_new, const void* v_new,
+                                   void* k_cache, void* v_cache, const int32_t* block_tables,
+                                   const int32_t* context_lens, int num_seqs, int num_queries,
+                                   int num_heads, int num_kv_heads, int head_size, int block_size,
+                                   int max_blocks_per_seq, float scale, void* stream, int dtype,
+                                   int num_physical_blocks, void* workspace, size_t workspace_bytes,
+                                   int num_ranges, int32_t* error_flag) {
+  if (k_new == nullptr || v_new == nullptr) {
+    pa::clear_error();
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_mq_append: null k_new / v_new");
+  }
+  return pa::decode_impl_q(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                           num_queries, num_heads, num_kv_heads, head_size, block_size,
+                           max_blocks_per_seq, scale, stream, dtype, num_physical_blocks, workspace,
+                           workspace_bytes, num_ranges, error_flag, false, 1.f, 1.f, k_new, v_new);
 }
 
 extern "C" size_t pa_decode_mq_workspace_size(int num_seqs, int num_queries, int num_heads,

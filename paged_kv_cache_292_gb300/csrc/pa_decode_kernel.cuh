@@ -31,8 +31,11 @@
 //     domain), then O^T[D x 8] += V^T[D x 16] * P^T[16 x 8], with P^T obtained
 //     from the score fragment by movmatrix.  FP8 pools: codes widened to f16
 //     (MmaConsumerF8).  fp32: the same on CUDA cores.
-//   * Appending calls also write each sequence's newest token: the consumer
-//     warps put it into the staged tile and into the pool (append_newest).
+//   * Appending calls also write the step's new tokens of each sequence: the
+//     consumer warps put them into the staged tile and into the pool
+//     (append_new_rows).  Not with two consumer warps per KV head, where that
+//     code slowed the consumers' tile loop: the host then writes the rows with
+//     a separate kernel ahead of the decode.
 //   * A sequence wholly inside the range is written to `out` directly.  A
 //     sequence cut by range boundaries leaves one (m, l, O) partial per range
 //     and KV head; the warp that writes the last of them (an atomic ticket per
@@ -72,16 +75,18 @@ struct StageMeta {
   int flags;   // kSegBegin | kSegEnd | (output slot + 1) << 2 | (slot of range r0) << 4
   int r0, r1;  // first and last range touching the sequence (cut sequences only)
   int ctx;     // the sequence's context length (causal limits of several queries)
-  int newrow;  // appending calls: pool row of the sequence's newest token when this
-               // tile holds it (at tile row nvalid - 1); else -1
+  int newfirst;  // appending calls: first tile row holding one of the step's new
+                 // tokens (rows newfirst .. nvalid-1; their pool rows are in the
+                 // stage's row list); -1 when the tile holds none
 };
 
 struct DecodeParams {
   CUtensorMap tm_k, tm_v;  // tensor-core paths: 4-D views of the pools (see make_tensor_maps)
   void* out;
-  // Appending calls (bf16, one query): K/V rows [num_seqs, num_kv_heads,
-  // head_size] of each sequence's newest token, written into the pool by the
-  // decode itself; nullptr otherwise.
+  // Appending calls (bf16, at most 8 (query, head) columns per KV head): K/V
+  // rows [num_seqs * num_queries, num_kv_heads, head_size] of each sequence's
+  // new tokens (row s * Q + i: position c - Q + i), written into the pool by
+  // the decode itself; nullptr otherwise.
   const void* k_new;
   const void* v_new;
   const void* q;
@@ -110,7 +115,7 @@ struct DecodeParams {
 };
 
 struct Layout {
-  uint32_t bar, meta, misc, qring, stage, total;
+  uint32_t bar, meta, rows, misc, qring, stage, total;
 };
 
 // Shared-memory carve-up; identical on host (sizing) and device (addressing).
@@ -125,6 +130,8 @@ PA_HD Layout make_layout(int stages, int q_slots, uint32_t q_bytes, uint32_t sta
   o = (o + 15u) & ~15u;
   L.meta = o;
   o += 32u * stages;
+  L.rows = o;  // per stage: pool row of each tile row holding a new token
+  o += 4u * kTile * stages;
   L.misc = o;
   o += 4u * 80u;
   o = (o + 127u) & ~127u;
@@ -835,11 +842,13 @@ struct SimtConsumer {
   }
 };
 
-// Zero output row of an empty sequence (16-byte stores; rows are 16-byte multiples).
+// Zero the output rows of an empty sequence (16-byte stores; rows are 16-byte multiples).
 template <typename T, int D>
 __device__ void zero_row(const DecodeParams& p, int s) {
-  const size_t n16 = (size_t)p.num_heads * D * sizeof(T) / 16;
-  uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) + (size_t)s * p.num_heads * D);
+  // Output rows of sequence s: [num_queries][num_heads][D].
+  const size_t n = (size_t)p.num_queries * p.num_heads * D;
+  const size_t n16 = n * sizeof(T) / 16;
+  uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<T*>(p.out) + (size_t)s * n);
   for (size_t i = 0; i < n16; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
@@ -962,30 +971,38 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
   if (lane == 0) *cnt = 0;  // leave the counter zeroed for the next call
 }
 
-// Appending calls: the tile holding a sequence's newest token (row
-// mt.nvalid - 1) may have been staged before that token reached the pool, so
-// the warp of KV head kv_head puts the token's K and V (from k_new / v_new)
-// into its own columns of the staged rows, swizzled as the tensor copy lays
-// them out, and also stores them into the pool row for later steps.  Lane u
-// < 16 moves 16-byte unit u of the K row, lane 16 + u the same unit of V.
+// Appending calls: a tile holding some of the step's new tokens (tile rows
+// mt.newfirst .. mt.nvalid - 1, query positions c - Q .. c - 1) may have been
+// staged before those tokens reached the pool, so the warp of KV head kv_head
+// puts each new token's K and V (from k_new / v_new, row s * Q + i for the
+// token at position c - Q + i) into its own columns of the staged rows,
+// swizzled as the tensor copy lays them out, and also stores them into the
+// token's pool row (rows[r]; -1 leaves it unwritten).  Lane u < 16 moves
+// 16-byte unit u of the K row, lane 16 + u the same unit of V.
 template <int D>
-__device__ __forceinline__ void append_newest(const DecodeParams& p, const StageMeta& mt, int kv_head,
-                                              int w, uint32_t k_half, uint32_t v_half, int lane) {
+__device__ __forceinline__ void append_new_rows(const DecodeParams& p, const StageMeta& mt, const int* rows,
+                                                int kv_head, int w, uint32_t k_half, uint32_t v_half,
+                                                int lane) {
   constexpr int UH = D * 2 / 16;  // 16-byte units of one head's bf16 row
   const int u = lane & 15;
   const bool is_v = lane >= 16;
-  if (u < UH) {
-    const size_t e = ((size_t)mt.seq * p.num_kv_heads + kv_head) * D + u * 8;
-    const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-        static_cast<const __nv_bfloat16*>(is_v ? p.v_new : p.k_new) + e));
-    const uint32_t unit = (uint32_t)(w * UH + u);
-    const uint32_t L = (uint32_t)(mt.nvalid - 1) * p.lines + (unit >> 3);
-    const uint32_t dst = (is_v ? v_half : k_half) + L * kLine + (((unit & 7u) ^ (L & 7u)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val.x), "r"(val.y),
-                 "r"(val.z), "r"(val.w)
-                 : "memory");
-    __nv_bfloat16* pool = static_cast<__nv_bfloat16*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache));
-    *reinterpret_cast<uint4*>(pool + ((size_t)mt.newrow * p.num_kv_heads + kv_head) * D + u * 8) = val;
+  const int Q = p.num_queries;
+  for (int r = mt.newfirst; r < mt.nvalid; ++r) {
+    const int prow = rows[r];
+    if (u < UH && prow >= 0) {
+      const size_t tok = (size_t)mt.seq * Q + (mt.tok0 + r - (mt.ctx - Q));  // row of k_new / v_new
+      const size_t e = (tok * p.num_kv_heads + kv_head) * D + u * 8;
+      const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(is_v ? p.v_new : p.k_new) + e));
+      const uint32_t unit = (uint32_t)(w * UH + u);
+      const uint32_t L = (uint32_t)r * p.lines + (unit >> 3);
+      const uint32_t dst = (is_v ? v_half : k_half) + L * kLine + (((unit & 7u) ^ (L & 7u)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(val.x), "r"(val.y),
+                   "r"(val.z), "r"(val.w)
+                   : "memory");
+      __nv_bfloat16* pool = static_cast<__nv_bfloat16*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache));
+      *reinterpret_cast<uint4*>(pool + ((size_t)prow * p.num_kv_heads + kv_head) * D + u * 8) = val;
+    }
   }
   // The stage is later refilled by the TMA engine (async proxy): order these
   // generic-proxy writes before that, and make them visible to the warp.
@@ -993,39 +1010,46 @@ __device__ __forceinline__ void append_newest(const DecodeParams& p, const Stage
   __syncwarp();
 }
 
-// The same for FP8 pools: the token's bf16 K/V are quantised exactly as the
-// FP8 cache write does (fp32 quotient by the pool's scale, E4M3 round to
-// nearest even, saturating), 16 codes per lane.
+// The same for FP8 pools (one query per sequence): the token's bf16 K/V are
+// quantised exactly as the FP8 cache write does (fp32 quotient by the pool's
+// scale, E4M3 round to nearest even, saturating), 16 codes per lane.
 template <int D>
-__device__ __forceinline__ void append_newest_fp8(const DecodeParams& p, const StageMeta& mt, int kv_head,
-                                                  int w, uint32_t k_half, uint32_t v_half, int lane) {
+__device__ __forceinline__ void append_new_rows_fp8(const DecodeParams& p, const StageMeta& mt,
+                                                    const int* rows, int kv_head, int w, uint32_t k_half,
+                                                    uint32_t v_half, int lane) {
   constexpr int UH = D / 16;  // 16-byte units of one head's FP8 row
   const int u = lane & 15;
   const bool is_v = lane >= 16;
-  if (u < UH) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(is_v ? p.v_new : p.k_new) +
-                                                      ((size_t)mt.seq * p.num_kv_heads + kv_head) * D + u * 16);
-    const uint4 a = __ldg(src), b = __ldg(src + 1);
-    const float sc = is_v ? p.v_scale : p.k_scale;
-    const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t out[4];
+  const int Q = p.num_queries;
+  for (int r = mt.newfirst; r < mt.nvalid; ++r) {
+    const int prow = rows[r];
+    if (u < UH && prow >= 0) {
+      const size_t tok = (size_t)mt.seq * Q + (mt.tok0 + r - (mt.ctx - Q));
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(is_v ? p.v_new : p.k_new) + (tok * p.num_kv_heads + kv_head) * D +
+          u * 16);
+      const uint4 a = __ldg(src), b = __ldg(src + 1);
+      const float sc = is_v ? p.v_scale : p.k_scale;
+      const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t out[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
-          make_float2(bf16_lo(in[2 * i]) / sc, bf16_hi(in[2 * i]) / sc), __NV_SATFINITE, __NV_E4M3));
-      const uint32_t hi = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
-          make_float2(bf16_lo(in[2 * i + 1]) / sc, bf16_hi(in[2 * i + 1]) / sc), __NV_SATFINITE, __NV_E4M3));
-      out[i] = lo | (hi << 16);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+            make_float2(bf16_lo(in[2 * i]) / sc, bf16_hi(in[2 * i]) / sc), __NV_SATFINITE, __NV_E4M3));
+        const uint32_t hi = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+            make_float2(bf16_lo(in[2 * i + 1]) / sc, bf16_hi(in[2 * i + 1]) / sc), __NV_SATFINITE, __NV_E4M3));
+        out[i] = lo | (hi << 16);
+      }
+      const uint32_t unit = (uint32_t)(w * UH + u);
+      const uint32_t L = (uint32_t)r * p.lines + (unit >> 3);
+      const uint32_t dst = (is_v ? v_half : k_half) + L * kLine + (((unit & 7u) ^ (L & 7u)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(out[0]), "r"(out[1]),
+                   "r"(out[2]), "r"(out[3])
+                   : "memory");
+      unsigned char* pool = static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache));
+      *reinterpret_cast<uint4*>(pool + ((size_t)prow * p.num_kv_heads + kv_head) * D + u * 16) =
+          make_uint4(out[0], out[1], out[2], out[3]);
     }
-    const uint32_t unit = (uint32_t)(w * UH + u);
-    const uint32_t L = (uint32_t)(mt.nvalid - 1) * p.lines + (unit >> 3);
-    const uint32_t dst = (is_v ? v_half : k_half) + L * kLine + (((unit & 7u) ^ (L & 7u)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(out[0]), "r"(out[1]), "r"(out[2]),
-                 "r"(out[3])
-                 : "memory");
-    unsigned char* pool = static_cast<unsigned char*>(const_cast<void*>(is_v ? p.v_cache : p.k_cache));
-    *reinterpret_cast<uint4*>(pool + ((size_t)mt.newrow * p.num_kv_heads + kv_head) * D + u * 16) =
-        make_uint4(out[0], out[1], out[2], out[3]);
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncwarp();
@@ -1100,6 +1124,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * NS + i); };
   auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + NQ + i); };
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta);
+  int* stage_rows = reinterpret_cast<int*>(smem + L.rows);
   int* abort_flag = reinterpret_cast<int*>(misc + 34);
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -1239,26 +1264,26 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       // consumers.  fp32: one bulk copy per valid token row.
       ok = ok && lead;
       const unsigned copies = __ballot_sync(0xffffffffu, ok);
+      // Token row of the pool: fewer than 2^31 in any pool that fits in device memory.
+      const int row = (int)((bs_sh >= 0 ? (unsigned)phys << bs_sh : (unsigned)phys * (unsigned)bs) +
+                            (unsigned)off_of(tok));
+      // Appending calls: the step's new tokens are positions c - Q .. c - 1.
+      int newfirst = -1;
+      if (kMmaPath && p.k_new != nullptr && tok0 + nvalid > c - p.num_queries) {
+        newfirst = max(0, c - p.num_queries - tok0);
+      }
       if (!mbar_wait(empty_bar(st), ph ^ 1u)) {
         report(p.error_flag, PA_DEVERR_TIMEOUT);
         break;
       }
-      // Token row of the pool: fewer than 2^31 in any pool that fits in device memory.
-      const int row = (int)((bs_sh >= 0 ? (unsigned)phys << bs_sh : (unsigned)phys * (unsigned)bs) +
-                            (unsigned)off_of(tok));
-      int newrow = -1;
-      if (kMmaPath && p.k_new != nullptr && tok0 + nvalid == c) {
-        // This tile holds the newest token (row nvalid - 1); a failed block
-        // check leaves it unwritten.
-        const int rn = __shfl_sync(0xffffffffu, row, nvalid - 1);
-        const int bad = __shfl_sync(0xffffffffu,
-                                    (int)(p.num_physical_blocks > 0 &&
-                                          (phys < 0 || phys >= p.num_physical_blocks)),
-                                    nvalid - 1);
-        newrow = bad ? -1 : rn;
+      if (newfirst >= 0 && !is_v && t >= newfirst && t < nvalid) {
+        // Pool row of this tile row's new token; a failed block check leaves it unwritten.
+        const bool bad = p.num_physical_blocks > 0 && (phys < 0 || phys >= p.num_physical_blocks);
+        stage_rows[st * kTile + t] = bad ? -1 : row;
       }
+      __syncwarp();
       if (lane == 0) {
-        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, c, newrow};
+        meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, c, newfirst};
         mbar_arrive_expect_tx(full_bar(st), __popc(copies) * (kMmaPath ? p.box_bytes : p.row_bytes));
       }
       __syncwarp();
@@ -1316,12 +1341,13 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const uint32_t k_half = stages + st * p.stage_bytes;
       const uint32_t v_half = k_half + kTile * p.lines * kLine;
       const int uh = w * D * kKVBytes / 16;  // this head's first 16-byte unit in the row
-      if constexpr (kMma && QMODE == 0) {
-        if (mt.newrow >= 0) {
+      if constexpr (kMma && QMODE < 2) {
+        if (mt.newfirst >= 0) {
+          const int* rows = stage_rows + st * kTile;
           if constexpr (KV8)
-            append_newest_fp8<D>(p, mt, kv_head, w, k_half, v_half, lane);
+            append_new_rows_fp8<D>(p, mt, rows, kv_head, w, k_half, v_half, lane);
           else
-            append_newest<D>(p, mt, kv_head, w, k_half, v_half, lane);
+            append_new_rows<D>(p, mt, rows, kv_head, w, k_half, v_half, lane);
         }
       }
       if constexpr (KV8) {

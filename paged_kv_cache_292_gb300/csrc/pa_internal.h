@@ -31,6 +31,14 @@ int library_workspace(size_t bytes, void** ptr);
 // to at least `bytes` (zero-filled again when it grows).
 int library_counters(size_t bytes, int32_t** ptr);
 
+// Writes the new rows of a multi-query appending call into the pools (token
+// i of sequence s at position context_lens[s] - num_queries + i), as its own
+// kernel launch on `stream`.  bf16 only; the caller validates the arguments.
+int append_rows_impl(const void* k_new, const void* v_new, const int32_t* block_tables,
+                     const int32_t* context_lens, void* k_cache, void* v_cache, int num_seqs,
+                     int num_queries, int num_kv_heads, int head_size, int block_size,
+                     int max_blocks_per_seq, int num_physical_blocks, void* stream, int32_t* error_flag);
+
 inline bool aligned(const void* p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

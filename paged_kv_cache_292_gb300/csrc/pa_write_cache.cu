@@ -88,6 +88,73 @@ int write_cache_impl(const void* k_new, const void* v_new, const int64_t* slot_m
   return PA_OK;
 }
 
+// The new rows of a multi-query appending call, for shapes whose decode does
+// not write them itself: token i of sequence s (row s * Q + i of k_new /
+// v_new) sits at position c - Q + i of its sequence, so its slot comes from
+// the block table.  Tokens before the sequence's start are skipped; lengths
+// outside [0, max_blocks_per_seq * block_size] are clamped as the decode
+// clamps them, and a failed block-id check (num_physical_blocks > 0) leaves
+// the token unwritten and sets PA_DEVERR_BLOCK_ID.  One CTA per token.
+__global__ void __launch_bounds__(128) pa_append_rows_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int32_t* __restrict__ block_tables,
+    const int32_t* __restrict__ context_lens, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+    int num_seqs, int num_queries, int block_size, int max_blocks_per_seq, int row_vecs,
+    int num_physical_blocks, int32_t* error_flag) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long n = (long long)num_seqs * num_queries;
+  for (long long i = blockIdx.x; i < n; i += gridDim.x) {
+    const int s = (int)(i / num_queries), qi = (int)(i % num_queries);
+    const int cmax = max_blocks_per_seq * block_size;
+    const int c = min(max(context_lens[s], 0), cmax);
+    const int pos = c - num_queries + qi;
+    if (pos < 0) continue;
+    const int blk = block_tables[(size_t)s * max_blocks_per_seq + pos / block_size];
+    if (num_physical_blocks > 0 && (blk < 0 || blk >= num_physical_blocks)) {
+      if (threadIdx.x == 0) report(error_flag, PA_DEVERR_BLOCK_ID);
+      continue;
+    }
+    const size_t slot = (size_t)blk * block_size + pos % block_size;
+    const uint4* ks = k_new + (size_t)i * row_vecs;
+    const uint4* vs = v_new + (size_t)i * row_vecs;
+    uint4* kd = k_cache + slot * row_vecs;
+    uint4* vd = v_cache + slot * row_vecs;
+    for (int j = threadIdx.x; j < row_vecs; j += blockDim.x) {
+      const uint4 kv = __ldg(ks + j);
+      const uint4 vv = __ldg(vs + j);
+      kd[j] = kv;
+      vd[j] = vv;
+    }
+  }
+}
+
+// Launches pa_append_rows_kernel (programmatic dependent launch, like the
+// cache write).  Arguments are validated by the caller (bf16 rows of
+// num_kv_heads * head_size elements, 16-byte aligned).
+int append_rows_impl(const void* k_new, const void* v_new, const int32_t* block_tables,
+                     const int32_t* context_lens, void* k_cache, void* v_cache, int num_seqs,
+                     int num_queries, int num_kv_heads, int head_size, int block_size,
+                     int max_blocks_per_seq, int num_physical_blocks, void* stream, int32_t* error_flag) {
+  const long long n = (long long)num_seqs * num_queries;
+  if (n <= 0) return PA_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n < 65535 ? n : 65535));
+  cfg.blockDim = dim3(128);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, pa_append_rows_kernel, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      block_tables, context_lens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_seqs,
+      num_queries, block_size, max_blocks_per_seq, num_kv_heads * head_size * 2 / 16, num_physical_blocks,
+      error_flag);
+  if (e != cudaSuccess) return cuda_fail(e, "launch pa_append_rows_kernel");
+  return PA_OK;
+}
+
 }  // namespace pa
 
 extern "C" int pa_write_cache(const void* k_new, const void* v_new, const int64_t* slot_mapping,

@@ -129,6 +129,25 @@ def test_decode_fp8_append_rejects_bad_arguments_on_host(lib, kw, code):
     assert rc == code
 
 
+@pytest.mark.parametrize(
+    "kw, code",
+    [
+        (dict(k_new=None), binding.PA_ERR_INVALID_ARG),
+        (dict(v_new=24), binding.PA_ERR_INVALID_ARG),  # misaligned
+        (dict(dtype=binding.PA_F32), binding.PA_ERR_UNSUPPORTED),
+        (dict(num_queries=0), binding.PA_ERR_INVALID_ARG),
+        (dict(num_queries=3), binding.PA_ERR_UNSUPPORTED),  # group 8 x 3 queries > 16
+    ],
+)
+def test_decode_mq_append_rejects_bad_arguments_on_host(lib, kw, code):
+    a = dict(k_new=16, v_new=16, dtype=binding.PA_BF16, num_queries=2)
+    a.update(kw)
+    rc = lib.pa_decode_mq_append(16, 16, a["k_new"], a["v_new"], 16, 16, 16, 16, 1, a["num_queries"], 32, 4, 128,
+                                 16, 4, 0.1, 0, a["dtype"], 0, None, 0, 0, None)
+    assert rc == code
+    assert lib.pa_last_error().decode()
+
+
 def test_workspace_size_formula(lib):
     def up(x):
         return (x + 255) // 256 * 256

@@ -99,6 +99,24 @@ def test_short_contexts_give_zero_rows_for_queries_before_the_start():
     assert torch.all(out[0, :3] == 0) and torch.all(out[2, :1] == 0)
 
 
+@pytest.mark.parametrize("Q", [2, 4])
+def test_empty_sequences_zero_all_their_query_rows(Q):
+    """A sequence with context 0 gets Q zero rows, and no other sequence's rows
+    are touched (the output starts as NaN)."""
+    ctx = np.array([5, 0, 40, 0, 17, 3, 0, 33])
+    sp = workloads.spec("llama3_8b", num_seqs=len(ctx), max_context=48, pool_blocks=0)
+    w = workloads.make_workload(sp, prewritten=True, poison=True, context_lens=ctx)
+    q = torch.randn(len(ctx), Q, 32, 128, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    g = to_device(w)
+    out = torch.full((len(ctx), Q, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    binding.decode_multi(q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"], g["context_lens"], w.scale,
+                         out=out)
+    torch.cuda.synchronize()
+    assert_close(out, _oracle(w, q), "bf16", f"empty sequences Q={Q}")
+    for s in np.flatnonzero(ctx == 0):
+        assert torch.all(out[s] == 0)
+
+
 def test_one_query_equals_pa_decode():
     w, q = _case("llama3_8b", 1, **SMALL_LLAMA)
     g = to_device(w)
