@@ -48,7 +48,7 @@ def _both(w, **kw):
 
 
 @pytest.mark.parametrize("name", list(CASES))
-@pytest.mark.parametrize("num_ranges", [0, 1, 997])
+@pytest.mark.parametrize("num_ranges", [0, 1, 5, 997])
 def test_append_equals_write_then_decode(name, num_ranges):
     w = workloads.make_workload(CASES[name], prewritten=False, poison=True)
     a, out_a, b, out_b = _both(w, num_ranges=num_ranges, check_block_ids=True)

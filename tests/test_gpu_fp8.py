@@ -75,7 +75,7 @@ SMALL = {
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-@pytest.mark.parametrize("num_ranges", [0, 1])
+@pytest.mark.parametrize("num_ranges", [0, 1, 5])
 def test_fp8_decode_matches_oracle(name, num_ranges):
     w = workloads.make_workload(SMALL[name], prewritten=True)
     k_scale, v_scale = 0.5, 0.25

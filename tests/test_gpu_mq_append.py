@@ -81,7 +81,7 @@ SMALL_LLAMA = dict(num_seqs=10, ctx_lo=1, ctx_hi=500, max_context=512, pool_bloc
 
 
 @pytest.mark.parametrize("Q", [1, 2, 4])
-@pytest.mark.parametrize("num_ranges", [0, 1, 997])
+@pytest.mark.parametrize("num_ranges", [0, 1, 5, 997])
 def test_mq_append_llama_shaped(Q, num_ranges):
     _check(workloads.spec("llama3_8b", **SMALL_LLAMA), Q, num_ranges, what=f"Q={Q} R={num_ranges}")
 
@@ -95,7 +95,7 @@ def test_mq_append_block_sizes(Q, block_size):
 # More than 8 (query, head) columns per KV head: two warps of a KV head patch
 # the same new rows.
 @pytest.mark.parametrize("heads, kv_heads, Q", [(8, 1, 2), (10, 2, 3), (32, 8, 3), (64, 8, 2)])
-@pytest.mark.parametrize("num_ranges", [0, 1])
+@pytest.mark.parametrize("num_ranges", [0, 1, 5])
 def test_mq_append_split_columns(heads, kv_heads, Q, num_ranges):
     sp = workloads.spec("llama3_8b", num_heads=heads, num_kv_heads=kv_heads, num_seqs=7, ctx_lo=1, ctx_hi=300,
                         max_context=304, pool_blocks=0)

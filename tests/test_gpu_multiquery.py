@@ -42,7 +42,7 @@ SMALL_LLAMA = dict(num_seqs=10, ctx_lo=1, ctx_hi=500, max_context=512, pool_bloc
 
 
 @pytest.mark.parametrize("Q", [1, 2, 3, 4])
-@pytest.mark.parametrize("num_ranges", [0, 1, 997])
+@pytest.mark.parametrize("num_ranges", [0, 1, 5, 997])
 def test_multi_query_llama_shaped(Q, num_ranges):
     w, q = _case("llama3_8b", Q, **SMALL_LLAMA)
     g = to_device(w)
@@ -75,7 +75,7 @@ def test_multi_query_block_sizes(Q, block_size):
 # More than 8 (query, head) columns per KV head: two warps per KV head, one of
 # them with padding columns when G * Q is not 16.
 @pytest.mark.parametrize("heads, kv_heads, Q", [(8, 1, 2), (12, 2, 2), (10, 2, 3), (32, 8, 3)])
-@pytest.mark.parametrize("num_ranges", [0, 1])
+@pytest.mark.parametrize("num_ranges", [0, 1, 5])
 def test_multi_query_split_columns(heads, kv_heads, Q, num_ranges):
     w, q = _case("llama3_8b", Q, seed=heads, num_heads=heads, num_kv_heads=kv_heads, num_seqs=7, ctx_lo=1,
                  ctx_hi=400, max_context=400, pool_blocks=0)
