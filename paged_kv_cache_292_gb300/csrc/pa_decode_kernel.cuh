@@ -409,19 +409,26 @@ struct MmaConsumerMQ {
   __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
                                        int nvalid, int tok0, int ctx, int G, int Q,
                                        float scale_log2, int lane) {
-    float c[NT][4];
+    // Scores accumulate in two independent chains (even / odd k-steps) that
+    // are added at the end: with one 8-column tile per warp, a single chain
+    // would serialise all KS MMAs.
+    float c[NT][4], c2[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
+      for (int i = 0; i < 4; ++i) c[nt][i] = c2[nt][i] = 0.f;
     const RowPtr<NC> kp(k_half, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
       ldmatrix_x4(a, kp.at(ks));
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(c[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816((ks & 1) ? c2[nt] : c[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[nt][i] += c2[nt][i];
     const int r0 = lane >> 2;
     const int t0 = tok0 + r0, t1 = t0 + 8;
     uint32_t pb0[NT], pb1[NT], rb0[NT], rb1[NT];
@@ -472,6 +479,21 @@ struct MmaConsumerMQ {
       keep_lo = (t2 < nvalid ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid ? 0xffff0000u : 0u);
       keep_hi = (t2 + 8 < nvalid ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid ? 0xffff0000u : 0u);
     }
+    // Rescale the accumulators only when some running max moved (a warp vote).
+    bool moved = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) moved |= (alpha_a[nt] != 1.f) || (alpha_b[nt] != 1.f);
+    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[nt][mt][0] *= alpha_a[nt];
+          acc[nt][mt][1] *= alpha_b[nt];
+          acc[nt][mt][2] *= alpha_a[nt];
+          acc[nt][mt][3] *= alpha_b[nt];
+        }
+    }
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       uint32_t a[4];
@@ -482,10 +504,6 @@ struct MmaConsumerMQ {
       a[3] &= keep_hi;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        acc[nt][mt][0] *= alpha_a[nt];
-        acc[nt][mt][1] *= alpha_b[nt];
-        acc[nt][mt][2] *= alpha_a[nt];
-        acc[nt][mt][3] *= alpha_b[nt];
         mma_bf16_16816(acc[nt][mt], a, pb0[nt], pb1[nt]);
         mma_bf16_16816(acc[nt][mt], a, rb0[nt], rb1[nt]);
       }
