@@ -42,7 +42,8 @@
 //     sequence and KV head, no waiting) then merges them all by log-sum-exp:
 //     out = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i.  The ticket counters
 //     are reset by that warp, so the scratch is left zeroed for the next call.
-//   * Empty sequences get a zero row from the prologue.
+//   * Empty sequences get zero output rows (all their query rows) from the
+//     prologue.
 #pragma once
 
 #include <cuda.h>
