@@ -29,6 +29,9 @@ def test_library_exports_every_header_symbol(lib):
     nm = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()], capture_output=True, text=True)
     exported = {line.split()[-1] for line in nm.stdout.splitlines() if " T " in line}
     assert set(names) <= exported
+    # ...and nothing else of the library's own: every exported pa_* symbol is
+    # declared (and documented) in a header.
+    assert {n for n in exported if n.startswith("pa_")} == set(names)
     assert lib.pa_version() == 100
 
 
