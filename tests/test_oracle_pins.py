@@ -438,3 +438,128 @@ def test_fp8_decode_is_decode_of_dequantised_pool():
     assert np.array_equal(out, ref)
     # Quantisation error stays within half an E4M3 step of the scaled values.
     assert np.max(np.abs(ofp8.e4m3_decode(kcode) * 0.5 - kc)) <= 0.5 * 0.5 * 2.0**-3 * np.max(np.abs(kc)) * 2
+
+
+# --- the quantiser: code of x / scale, quotient in fp32 ------------------------
+#
+# The pages name quantised KV caches without a format; the reading is E4M3 codes
+# with one fp32 scale per pool, each code the nearest to the fp32 quotient
+# x / scale.  These pins hold `quantize` and `write_cache_fp8` to facts that
+# do not go through them: hand-derived codes, the fp32/exact quotient split at
+# tie points, torch's own E4M3 cast of the fp32 quotient, and the scatter's
+# byte-for-byte locality.  A quantiser that multiplies by the scale, divides in
+# fp64, or loses the sign of a zero fails at least one of them.
+
+
+def _f32(bits: int) -> np.float32:
+    return np.array([bits], dtype=np.uint32).view(np.float32)[0]
+
+
+def test_quantize_hand_derived_codes():
+    # 100 / 4 = 25 = 16 * 1.5625: halfway between 1.5 (mantissa 100) and 1.625
+    # (101), ties to the even mantissa: 24 = exponent field 4 + 7 = 1011, code
+    # 0 1011 100.  (100 * 4 = 400 would give 384, code 0x7C.)
+    assert ofp8.quantize(np.array([100.0]), 4.0)[0] == 0x5C
+    # 1000 / 4 = 250 lies between 240 (0x77) and 256 (0x78) and is nearer 256.
+    # (1000 * 4 saturates to 448, code 0x7E.)
+    assert ofp8.quantize(np.array([1000.0]), 4.0)[0] == 0x78
+    # Saturation keeps the sign: -1e6 / 0.5 -> -448.
+    assert ofp8.quantize(np.array([-1e6]), 0.5)[0] == 0xFE
+    # 3 / 0.75 = 4 exactly (2^2: exponent field 9 = 1001, mantissa 000).
+    assert ofp8.quantize(np.array([3.0]), 0.75)[0] == 0x48
+
+
+def test_quantize_keeps_the_sign_of_zero():
+    # Quotients that round to zero keep the input's sign bit, as IEEE rounding
+    # does: -0 -> 0x80, a negative value below half the smallest subnormal
+    # (2^-10) -> 0x80, a positive one -> 0x00.
+    codes = ofp8.quantize(np.array([-0.0, -1e-30, -2.0**-12, 0.0, 1e-30, 2.0**-12]), 2.0)
+    assert list(codes) == [0x80, 0x80, 0x80, 0x00, 0x00, 0x00]
+
+
+def test_quantize_power_of_two_scales_are_exact_reciprocals():
+    # Dividing by 2^k is exact in fp32 (no overflow or underflow here), so the
+    # code is the encoder's code of x * 2^-k, whatever the rounding precision.
+    rng = np.random.default_rng(40)
+    x = (rng.standard_normal(5000) * 30).astype(np.float32)
+    for k in (-3, -1, 0, 2, 5):
+        s = 2.0**k
+        want = ofp8.e4m3_encode(x.astype(np.float64) * 2.0**-k)
+        assert np.array_equal(ofp8.quantize(x, s), want), k
+
+
+# fp32 pairs (x, s), as bit patterns, whose exact quotient x / s lies within
+# half an fp32 ulp of an E4M3 tie point (the midpoint of two neighbouring
+# codes): the fp32 quotient lands exactly on the tie and rounds to the even
+# code, while the exact (or fp64) quotient is off the tie and rounds to the
+# other neighbour.  Found by searching random fp32 pairs; each row re-derives
+# its own premises below with exact rational arithmetic.
+#   (x bits, s bits, tie point, code of the fp32 quotient, code of the exact one)
+FP32_TIE_CASES = [
+    # 1.0625 is halfway between 1.0 (0x38, mantissa 000) and 1.125 (0x39).
+    (1071955372, 1071073562, 1.0625, 0x38, 0x39),
+    (1078126519, 1077375148, 1.0625, 0x38, 0x39),
+    # 1.1875 is halfway between 1.125 (0x39) and 1.25 (0x3A, mantissa 010).
+    (1062307510, 1060139377, 1.1875, 0x3A, 0x39),
+    (1071338826, 1069069213, 1.1875, 0x3A, 0x39),
+    # 3.5 * 2^-9 is halfway between the subnormals 3 * 2^-9 (0x03) and 4 * 2^-9 (0x04).
+    (1011338257, 1071929071, 0.0068359375, 0x04, 0x03),
+    # Negative: -1.0625 between -1.0 (0xB8) and -1.125 (0xB9).
+    (3218035470, 1069752574, -1.0625, 0xB8, 0xB9),
+]
+
+
+@pytest.mark.parametrize("xb, sb, tie, code32, code_exact", FP32_TIE_CASES)
+def test_quantize_divides_in_fp32_at_tie_points(xb, sb, tie, code32, code_exact):
+    from fractions import Fraction
+
+    x, s = _f32(xb), _f32(sb)
+    # Premises: the fp32 quotient is the tie itself, the exact one is not.
+    assert float(np.float32(x) / np.float32(s)) == tie
+    exact = Fraction(float(x)) / Fraction(float(s))
+    assert exact != Fraction(tie)
+    # The two codes are the tie's neighbours, and the exact quotient lies
+    # strictly between the tie and code_exact's value, so it rounds there.
+    v32, vex = ofp8.e4m3_decode(np.array([code32, code_exact], dtype=np.uint8))
+    assert Fraction(tie) == (Fraction(v32) + Fraction(vex)) / 2
+    assert min(Fraction(tie), Fraction(vex)) < exact < max(Fraction(tie), Fraction(vex))
+    # The reading: the code is decided on the fp32 quotient.
+    assert ofp8.quantize(np.array([x]), float(s))[0] == code32
+
+
+def test_quantize_matches_torch_cast_of_the_fp32_quotient():
+    """torch's E4M3 cast (round to nearest even from fp32) of the fp32
+    quotient, for quotients inside +-448 where torch does not produce NaN."""
+    rng = np.random.default_rng(41)
+    x = np.concatenate([rng.standard_normal(20000) * 3, rng.uniform(-200, 200, 3000),
+                        rng.standard_normal(3000) * 1e-2]).astype(np.float32)
+    for s in (0.37, 1.0, 2.5, 1e-3 * 7.3, 0.0913):
+        sf = np.float32(s)
+        quot = x / sf
+        keep = np.abs(quot) <= 448
+        ref = torch.from_numpy(quot[keep]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(ofp8.quantize(x[keep], s), ref), s
+
+
+def test_write_cache_fp8_scatters_torch_codes_and_nothing_else():
+    rng = np.random.default_rng(42)
+    nb, bs, hk, d, t = 9, 4, 2, 8, 11
+    kc = rng.integers(0, 256, (nb, bs, hk, d)).astype(np.uint8)
+    vc = rng.integers(0, 256, (nb, bs, hk, d)).astype(np.uint8)
+    kn = (rng.standard_normal((t, hk, d)) * 2).astype(np.float32)
+    vn = (rng.standard_normal((t, hk, d)) * 2).astype(np.float32)
+    slots = rng.permutation(nb * bs)[:t].astype(np.int64)
+    slots[[3, 7]] = -1
+    ks, vs = 0.37, 2.5
+    k2, v2 = ofp8.write_cache_fp8(kc, vc, kn, vn, slots, bs, ks, vs)
+
+    def cast(a, s):
+        return torch.from_numpy(a / np.float32(s)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+    kwant, vwant = kc.copy(), vc.copy()
+    for i, sl in enumerate(slots.tolist()):
+        if sl >= 0:
+            kwant[sl // bs, sl % bs] = cast(kn[i], ks)
+            vwant[sl // bs, sl % bs] = cast(vn[i], vs)
+    assert np.array_equal(k2, kwant) and np.array_equal(v2, vwant)
+    assert k2.dtype == np.uint8
