@@ -256,13 +256,17 @@ int pa_write_cache_ex(const void* k_new, const void* v_new, const int64_t* slot_
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
+ *   - Arguments are checked as pa_decode checks them, with the same return
+ *     codes; a rejected call queues nothing on `stream`.
  *   - All calls share the one array, which keeps the previous call's
- *     contents; each call clears the part that must start at zero (with
- *     cudaMemsetAsync on `stream`) before its kernel.  Calls that overlap in
- *     time on the GPU (different streams, no ordering) race on the array.
- *   - Batches whose scratch (pa_decode_workspace_size(num_seqs, num_heads,
- *     num_kv_heads, head_size, 0)) exceeds PA_STATIC_SCRATCH_BYTES are
- *     rejected with PA_ERR_WORKSPACE before anything is launched.
+ *     contents; each accepted call clears the part that must start at zero
+ *     (cudaMemsetAsync on `stream`) right before its kernel.  Calls that
+ *     overlap in time on the GPU (different streams, no ordering) race on
+ *     the array.
+ *   - Batches whose scratch exceeds PA_STATIC_SCRATCH_BYTES are rejected with
+ *     PA_ERR_WORKSPACE before anything is queued (the scratch is at most
+ *     pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, 0)
+ *     bytes: about 5 MB for 64 sequences of 32 query / 8 KV heads of 128).
  */
 #define PA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int pa_decode_static(void* out, const void* query, const void* k_cache, const void* v_cache,
@@ -312,6 +316,26 @@ int pa_decode_fp8_append(void* out, const void* query, const void* k_new, const 
                          int head_size, int block_size, int max_blocks_per_seq, float scale,
                          float k_scale, float v_scale, void* stream, int num_physical_blocks,
                          void* workspace, size_t workspace_bytes, int num_ranges, int32_t* error_flag);
+
+/*
+ * pa_test_stall_copy - test hook for the decode kernel's bounded waits; the
+ * pages have no counterpart.  Every wait of the decode pipeline (a consumer
+ * waiting for a stage's copies, the copy engine's issuer waiting for a free
+ * stage) gives up after a time limit, sets PA_DEVERR_TIMEOUT in error_flag and
+ * ends the kernel early, so that a copy that never lands cannot hang the GPU.
+ * This hook lets a test reach that path without any fault: the next decode
+ * call on the calling thread that launches its kernel (pa_decode*, any
+ * variant) withholds every copy of flattened tile `tile` (the batch's tiles of
+ * 16 tokens, sequence after sequence, counted from 0) and bounds every wait by
+ * wait_limit_us microseconds (0: the default of 2 s).  The stage meant for
+ * that tile is never filled, the waits on it run out, and the kernel returns
+ * after letting the copies it had started land (again within the limit).
+ * That call's output is unspecified, and its scratch (pa_decode_ws) must be
+ * zero-filled again before reuse.  The setting is used by one launch and then
+ * cleared; tile = -1 clears it.  Returns PA_OK, or PA_ERR_INVALID_ARG for
+ * tile < -1.
+ */
+int pa_test_stall_copy(long long tile, unsigned int wait_limit_us);
 
 /* Message for the calling thread's last non-zero return ("" if none). */
 const char* pa_last_error(void);

@@ -97,6 +97,7 @@ _SIGS = {
     "pa_bm_export": (_I, [_P, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _I]),
     "pa_version": (_I, []),
+    "pa_test_stall_copy": (_I, [ctypes.c_longlong, ctypes.c_uint]),
 }
 
 
@@ -259,6 +260,11 @@ def pa_last_error() -> str:
 
 def pa_version() -> int:
     return int(load().pa_version())
+
+
+def pa_test_stall_copy(tile: int, wait_limit_us: int = 0) -> None:
+    """Test hook: the next decode launch on this thread withholds tile `tile`'s copies and bounds its waits."""
+    _check(load().pa_test_stall_copy(tile, wait_limit_us))
 
 
 # ---- shape-derived conveniences ---------------------------------------------

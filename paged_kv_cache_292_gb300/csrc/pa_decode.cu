@@ -273,13 +273,19 @@ int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
 
 }  // namespace
 
+// fixed_scratch: when set and `workspace` is NULL, the scratch comes from this
+// provider (given the plan's byte count, it returns a device buffer that keeps
+// earlier contents, or an error) instead of the library's growable buffer;
+// its merge tickets are then cleared on `stream` right before the launch,
+// after every check has passed.
 int decode_impl_q(void* out, const void* query, const void* k_cache, const void* v_cache,
                   const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                   int num_queries, int num_heads, int num_kv_heads, int head_size, int block_size,
                   int max_blocks_per_seq, float scale, void* stream, int dtype,
                   int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
                   int32_t* error_flag, bool kv_fp8 = false, float k_scale = 1.f,
-                  float v_scale = 1.f, const void* k_new = nullptr, const void* v_new = nullptr) {
+                  float v_scale = 1.f, const void* k_new = nullptr, const void* v_new = nullptr,
+                  ScratchProvider fixed_scratch = nullptr) {
   clear_error();
   if (k_new != nullptr || v_new != nullptr) {
     if (k_new == nullptr || v_new == nullptr)
@@ -315,6 +321,12 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
                  num_queries, elt, block_size);
   if (rc != PA_OK) return rc;
   int32_t* counters = nullptr;
+  const bool clear_tickets = workspace == nullptr && fixed_scratch != nullptr;
+  if (clear_tickets) {
+    rc = fixed_scratch(pl.ws_total, &workspace);
+    if (rc != PA_OK) return rc;
+    workspace_bytes = pl.ws_total;
+  }
   if (workspace == nullptr) {
     rc = library_workspace(pl.ws_partials, &workspace);
     if (rc != PA_OK) return rc;
@@ -372,6 +384,12 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   prm.k_new = k_new;
   prm.v_new = v_new;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (clear_tickets) {
+    const cudaError_t e =
+        cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)num_seqs * num_kv_heads, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(merge tickets)");
+  }
+  take_wait_test(&prm.stall_tile, &prm.wait_limit_ns);
   if (k_new != nullptr && pl.split == 2) {
     // Two consumer warps per KV head: the rows are written by their own
     // kernel, chained ahead of the decode, which then only reads them.

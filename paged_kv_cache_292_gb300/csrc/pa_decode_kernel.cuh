@@ -113,6 +113,8 @@ struct DecodeParams {
   uint32_t box_rows;   // token rows per tensor copy: gcd(block_size, 16)
   uint32_t box_bytes;  // bytes one tensor copy lands (box_rows * lines * 128)
   float scale_log2;    // scale * log2(e)
+  unsigned long long wait_limit_ns;  // bound of every pipeline wait
+  long long stall_tile;  // tests of the bounded waits: flattened tile whose copies are withheld (-1: none)
 };
 
 struct Layout {
@@ -1144,7 +1146,14 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * NS + NQ + i); };
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta);
   int* stage_rows = reinterpret_cast<int*>(smem + L.rows);
-  int* abort_flag = reinterpret_cast<int*>(misc + 34);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 34);
+  // A pipeline wait ran out: report it and tell the producer to drain.
+  auto timed_out = [&]() {
+    if (lane == 0) {
+      report(p.error_flag, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  };
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full_bar(i), 1);
@@ -1182,6 +1191,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     int slot = 0, seg_r0 = 0, seg_r1 = 0, seg_slot0 = 0;
     int st = 0, qi = 0;
     uint32_t ph = 0, qph = 0;
+    long long armed = 0, q_armed = 0;  // stages and query slots armed so far
     const int t = lane & 15;
     const bool is_v = lane >= 16;
     if (kMmaPath && lane == 0) {
@@ -1241,8 +1251,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
                         ((slot + 1) << 2) | (seg_slot0 << 4);
       if (new_seq) {
-        if (!mbar_wait(qempty_bar(qi), qph ^ 1u)) {
-          report(p.error_flag, PA_DEVERR_TIMEOUT);
+        if (!mbar_wait_warp(qempty_bar(qi), qph ^ 1u, p.wait_limit_ns)) {
+          timed_out();
           break;
         }
         if (lane == 0) {
@@ -1260,6 +1270,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
                             per_q, qb);
           }
         }
+        ++q_armed;
         if (++qi == NQ) {
           qi = 0;
           qph ^= 1u;
@@ -1291,22 +1302,25 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       if (kMmaPath && p.k_new != nullptr && tok0 + nvalid > c - p.num_queries) {
         newfirst = max(0, c - p.num_queries - tok0);
       }
-      if (!mbar_wait(empty_bar(st), ph ^ 1u)) {
-        report(p.error_flag, PA_DEVERR_TIMEOUT);
+      if (!mbar_wait_warp(empty_bar(st), ph ^ 1u, p.wait_limit_ns)) {
+        timed_out();
         break;
       }
+      // Tests of the bounded waits: this tile's stage is never armed or
+      // filled, so the consumers' wait on it runs out.
+      const bool stall = x == p.stall_tile;
       if (newfirst >= 0 && !is_v && t >= newfirst && t < nvalid) {
         // Pool row of this tile row's new token; a failed block check leaves it unwritten.
         const bool bad = p.num_physical_blocks > 0 && (phys < 0 || phys >= p.num_physical_blocks);
         stage_rows[st * kTile + t] = bad ? -1 : row;
       }
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && !stall) {
         meta[st] = StageMeta{s, tok0, nvalid, flags, seg_r0, seg_r1, c, newfirst};
         mbar_arrive_expect_tx(full_bar(st), __popc(copies) * (kMmaPath ? p.box_bytes : p.row_bytes));
       }
       __syncwarp();
-      if (ok) {
+      if (ok && !stall) {
         const uint32_t dst = stages + st * p.stage_bytes + lane_dst;
         if constexpr (kMmaPath) {
           tma_load_4d(dst, tmap, 0, 0, hg, row, full_bar(st));
@@ -1315,10 +1329,22 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
           bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
         }
       }
+      ++armed;
       if (++st == NS) {
         st = 0;
         ph ^= 1u;
       }
+    }
+    named_barrier_sync(1, nthreads);  // every warp has left its tile loop
+    if (*abort_flag != 0 && lane == 0) {
+      // A wait ran out, so the loops ended early and copies this warp started
+      // may still be landing.  Wait (again bounded) for the last phase armed on
+      // every stage and query slot, so that no copy writes into this CTA's
+      // shared memory after it has retired.
+      for (int i = 0; i < NS; ++i)
+        if (armed > i) (void)mbar_wait(full_bar(i), i < st ? ph : ph ^ 1u, p.wait_limit_ns);
+      for (int i = 0; i < NQ; ++i)
+        if (q_armed > i) (void)mbar_wait(qfull_bar(i), i < qi ? qph : qph ^ 1u, p.wait_limit_ns);
     }
   } else {
     // ---------------- consumers ----------------
@@ -1334,14 +1360,14 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
     if constexpr (KV8) cons.setup(p.lines, w * D / 16, lane);
     for (long long x = a; x < b; ++x) {
-      if (!mbar_wait(full_bar(st), ph)) {
-        report(p.error_flag, PA_DEVERR_TIMEOUT);
+      if (!mbar_wait_warp(full_bar(st), ph, p.wait_limit_ns)) {
+        timed_out();
         break;
       }
       const StageMeta mt = meta[st];
       if (mt.flags & kSegBegin) {
-        if (!mbar_wait(qfull_bar(qi), qph)) {
-          report(p.error_flag, PA_DEVERR_TIMEOUT);
+        if (!mbar_wait_warp(qfull_bar(qi), qph, p.wait_limit_ns)) {
+          timed_out();
           break;
         }
         if constexpr (QMODE == 0 || KV8)
@@ -1394,8 +1420,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         ph ^= 1u;
       }
     }
+    named_barrier_sync(1, nthreads);  // lets the producer drain its copies after a timeout
   }
-  (void)abort_flag;
   (void)Hk;
 }
 

@@ -56,17 +56,31 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  The wait is
-// bounded: after kWaitLimitNs of wall time it gives up and returns false so
-// the caller can record PA_DEVERR_TIMEOUT and leave instead of hanging.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// bounded: after `limit_ns` of wall time it gives up and returns false so the
+// caller can record PA_DEVERR_TIMEOUT and leave instead of hanging.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default limit: 2 s
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t spin = 1;; ++spin) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((spin & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((spin & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The same wait taken by a whole warp, with one answer for every lane: each
+// lane's own limit could run out on either side of the phase completing, and
+// a warp whose lanes split there would leave some of them behind at the next
+// full-warp shuffle or barrier.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
+}
+
+// Named CTA barrier `id` over `nthreads` threads (a multiple of 32); the
+// threads may reach it from different places in the code.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---- bulk async copy global -> shared (completes on an mbarrier) -----------

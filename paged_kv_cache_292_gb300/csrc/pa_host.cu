@@ -13,6 +13,9 @@ namespace pa {
 
 namespace {
 thread_local char g_message[512] = {0};
+// pa_test_stall_copy: consumed by the next decode launch on this thread.
+thread_local long long g_stall_tile = -1;
+thread_local unsigned int g_stall_limit_us = 0;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -118,7 +121,22 @@ int library_counters(size_t bytes, int32_t** ptr) {
   return PA_OK;
 }
 
+void take_wait_test(long long* stall_tile, unsigned long long* wait_limit_ns) {
+  *stall_tile = g_stall_tile;
+  *wait_limit_ns = g_stall_limit_us ? 1000ull * g_stall_limit_us : 2000000000ull;
+  g_stall_tile = -1;
+  g_stall_limit_us = 0;
+}
+
 }  // namespace pa
+
+extern "C" int pa_test_stall_copy(long long tile, unsigned int wait_limit_us) {
+  pa::clear_error();
+  if (tile < -1) return pa::fail(PA_ERR_INVALID_ARG, "pa_test_stall_copy: tile %lld < -1", tile);
+  pa::g_stall_tile = tile;
+  pa::g_stall_limit_us = tile < 0 ? 0u : wait_limit_us;
+  return PA_OK;
+}
 
 extern "C" const char* pa_last_error(void) { return pa::g_message; }
 

@@ -39,6 +39,15 @@ int append_rows_impl(const void* k_new, const void* v_new, const int32_t* block_
                      int num_queries, int num_kv_heads, int head_size, int block_size,
                      int max_blocks_per_seq, int num_physical_blocks, void* stream, int32_t* error_flag);
 
+// The settings of pa_test_stall_copy for the decode launch about to be made on
+// this thread (then cleared): the tile whose copies are withheld (-1: none)
+// and the bound of every pipeline wait in nanoseconds.
+void take_wait_test(long long* stall_tile, unsigned long long* wait_limit_ns);
+
+// Supplies fixed (never allocated) decode scratch of at least `bytes` on the
+// current device, or returns an error code (PA_ERR_WORKSPACE when too small).
+typedef int (*ScratchProvider)(size_t bytes, void** ptr);
+
 inline bool aligned(const void* p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

@@ -25,23 +25,28 @@ static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_SCRATC
 
 namespace pa {
 
-int decode_impl(void* out, const void* query, const void* k_cache, const void* v_cache,
-                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
-                int num_heads, int num_kv_heads, int head_size, int block_size,
-                int max_blocks_per_seq, float scale, void* stream, int dtype,
-                int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
-                int32_t* error_flag);
-size_t decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
-                             int num_ranges);
+int decode_impl_q(void* out, const void* query, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                  int num_queries, int num_heads, int num_kv_heads, int head_size, int block_size,
+                  int max_blocks_per_seq, float scale, void* stream, int dtype,
+                  int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                  int32_t* error_flag, bool kv_fp8, float k_scale, float v_scale, const void* k_new,
+                  const void* v_new, ScratchProvider fixed_scratch);
 
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mutex;
 void* g_static_ptr[kMaxDevices] = {nullptr};
 
-// Device address of the scratch array on the current device (set up once per
-// device, with that device current).
-int static_scratch(void** ptr) {
+// The scratch array as the decode's fixed scratch: rejects batches that need
+// more than it holds, and returns its device address on the current device
+// (looked up once per device, with that device current).
+int static_scratch(size_t bytes, void** ptr) {
+  if (bytes > (size_t)PA_STATIC_SCRATCH_BYTES)
+    return fail(PA_ERR_WORKSPACE,
+                "pa_decode_static: this batch needs %zu bytes of scratch, more than the %zu "
+                "compiled in (use pa_decode or pa_decode_ws)",
+                bytes, (size_t)PA_STATIC_SCRATCH_BYTES);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -60,31 +65,17 @@ int static_scratch(void** ptr) {
 
 }  // namespace pa
 
+// The arguments are checked exactly as pa_decode checks them (same codes, and
+// nothing is queued on the stream for a rejected call); the scratch array then
+// stands in for the library's buffer, and its merge tickets are cleared on the
+// caller's stream just before the kernel.
 extern "C" int pa_decode_static(void* out, const void* query, const void* k_cache,
                                 const void* v_cache, const int32_t* block_tables,
                                 const int32_t* context_lens, int num_seqs, int num_heads,
                                 int num_kv_heads, int head_size, int block_size,
                                 int max_blocks_per_seq, float scale, void* stream, int dtype) {
-  pa::clear_error();
-  const size_t need = pa::decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, 0);
-  if (need == 0)
-    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_static: invalid sizes (or no usable device)");
-  if (need > (size_t)PA_STATIC_SCRATCH_BYTES)
-    return pa::fail(PA_ERR_WORKSPACE,
-                    "pa_decode_static: this batch needs %zu bytes of scratch, more than the %zu "
-                    "compiled in (use pa_decode or pa_decode_ws)",
-                    need, (size_t)PA_STATIC_SCRATCH_BYTES);
-  void* scratch = nullptr;
-  int rc = pa::static_scratch(&scratch);
-  if (rc != PA_OK) return rc;
-  // The merge tickets (in the scratch's last bytes for this batch shape) must
-  // start at zero; the array keeps whatever the previous call left, so clear
-  // them on the caller's stream first.
-  const size_t tickets = pa::align_up(sizeof(int32_t) * (size_t)num_seqs * num_kv_heads, 256);
-  cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - tickets), 0,
-                                  tickets, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return pa::cuda_fail(e, "cudaMemsetAsync(static scratch tickets)");
-  return pa::decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                         num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
-                         stream, dtype, 0, scratch, need, 0, nullptr);
+  return pa::decode_impl_q(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, 1,
+                           num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
+                           stream, dtype, 0, nullptr, 0, 0, nullptr, false, 1.f, 1.f, nullptr,
+                           nullptr, pa::static_scratch);
 }

@@ -59,9 +59,11 @@ def _decode_args(**kw):
         (dict(head_size=256), binding.PA_ERR_UNSUPPORTED),
     ],
 )
-def test_decode_rejects_bad_arguments_on_host(lib, kw, code):
+@pytest.mark.parametrize("entry", ["pa_decode", "pa_decode_static"])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, code, entry):
+    """pa_decode_static checks its arguments as pa_decode does, with the same codes."""
     a = _decode_args(**kw)
-    rc = lib.pa_decode(a["out"], a["query"], a["k_cache"], a["v_cache"], a["block_tables"], a["context_lens"],
+    rc = getattr(lib, entry)(a["out"], a["query"], a["k_cache"], a["v_cache"], a["block_tables"], a["context_lens"],
                        a["num_seqs"], a["num_heads"], a["num_kv_heads"], a["head_size"], a["block_size"],
                        a["max_blocks_per_seq"], a["scale"], a["stream"], a["dtype"])
     assert rc == code
@@ -172,3 +174,10 @@ def test_schedule_partition_host_check(tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, out.stdout + out.stderr
     assert out.stdout.startswith("ok")
+
+
+def test_stall_hook_checks_its_argument(lib):
+    """The bounded-wait test hook only records a setting on the host."""
+    assert lib.pa_test_stall_copy(-2, 0) == binding.PA_ERR_INVALID_ARG
+    assert lib.pa_test_stall_copy(5, 1000) == binding.PA_OK
+    assert lib.pa_test_stall_copy(-1, 0) == binding.PA_OK  # cleared

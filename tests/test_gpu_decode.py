@@ -219,10 +219,23 @@ FULL = [("llama3_8b", None, [0, 7, 21, 40, 63]), ("long_ctx", None, [0, 5]),
 
 @pytest.mark.parametrize("name, bs, sample", FULL)
 def test_full_size_sampled(name, bs, sample):
+    """Every full-size batch in both launch forms: the fused step the benchmark
+    times (pa_decode_append, one launch) and pa_write_cache + pa_decode.  The
+    two give bit-identical pools and outputs; the written rows are the new
+    tokens bit for bit; sampled sequences (the longest always among them)
+    match the oracle."""
     w = workloads.make_workload(name, block_size=bs, prewritten=False)
     g, out = _write_then_decode(w)
-    # Written rows are the new tokens, bit for bit.
+    f = to_device(w)
+    out_f = binding.decode_append(f["q"], f["k_new"], f["v_new"], f["k_cache"], f["v_cache"], f["block_tables"],
+                                  f["context_lens"], w.scale)
+    torch.cuda.synchronize()
     view = int_view(w.spec.dtype)
+    assert torch.equal(out_f.view(view), out.view(view))
+    assert torch.equal(f["k_cache"].view(view), g["k_cache"].view(view))
+    assert torch.equal(f["v_cache"].view(view), g["v_cache"].view(view))
+    del f
+    # Written rows are the new tokens, bit for bit.
     b = w.spec.block_size
     for s in sample:
         slot = int(w.slot_mapping[s])
@@ -235,4 +248,5 @@ def test_full_size_sampled(name, bs, sample):
     sample = sorted(set(sample) | {longest})
     want = oracle_decode(w, k_ref, v_ref, seqs=sample)
     assert_close(out[sample], want, w.spec.dtype, name)
+    assert_close(out_f[sample], want, w.spec.dtype, name + " (fused step)")
     assert torch.isfinite(out).all()

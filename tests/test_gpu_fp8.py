@@ -142,3 +142,67 @@ def test_fp8_append_equals_write_then_decode(name, num_ranges):
     torch.cuda.synchronize()
     assert torch.equal(kb, ka) and torch.equal(vb, va)
     assert torch.equal(out_b.view(torch.int16), out_a.view(torch.int16))
+
+
+# ---- full size, in the launch form the benchmark times ----
+
+
+def _compact(w, codes, seqs):
+    """The sampled sequences' blocks of a code pool, relabelled 0.., with their
+    tables, lengths and the local slot of each one's newest token."""
+    bs = w.spec.block_size
+    bt, ctx = w.block_tables.numpy(), w.context_lens.numpy()
+    nblk = [-(-int(ctx[s]) // bs) for s in seqs]
+    used = sorted({int(b) for s, n in zip(seqs, nblk) for b in bt[s, :n]})
+    remap = {b: i for i, b in enumerate(used)}
+    bt2 = np.full((len(seqs), max(nblk)), -1, dtype=np.int64)
+    slots = np.full(len(seqs), -1, dtype=np.int64)
+    for i, (s, n) in enumerate(zip(seqs, nblk)):
+        bt2[i, :n] = [remap[int(b)] for b in bt[s, :n]]
+        c = int(ctx[s])
+        slots[i] = remap[int(bt[s, (c - 1) // bs])] * bs + (c - 1) % bs
+    return codes[torch.as_tensor(used)].numpy(), bt2, ctx[seqs], slots
+
+
+@pytest.mark.parametrize("name, sample", [("llama3_8b", [0, 7, 21, 40, 63]), ("long_ctx", [0, 3, 7])])
+def test_full_size_fp8_append_sampled(name, sample):
+    """pa_decode_fp8_append on the full batch: bit-identical to
+    pa_write_cache_fp8 + pa_decode_fp8, the written codes equal the oracle's
+    quantiser, and sampled sequences (the longest among them) match the oracle
+    on the oracle-written pools.  The prompt's codes are torch's E4M3 cast of
+    the pool over its scale (input generation)."""
+    w = workloads.make_workload(name, prewritten=False)
+    k_scale, v_scale = 0.37, 2.5
+    kin = (w.k_cache.cuda().float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    vin = (w.v_cache.cuda().float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    longest = int(torch.argmax(w.context_lens))
+    sample = sorted(set(sample) | {longest})
+    bs = w.spec.block_size
+    used_ids = torch.as_tensor(sorted({int(b) for s in sample
+                                       for b in w.block_tables[s, :-(-int(w.context_lens[s]) // bs)]}))
+    k_before = torch.zeros_like(w.k_cache, dtype=torch.uint8)
+    v_before = torch.zeros_like(w.v_cache, dtype=torch.uint8)
+    k_before[used_ids] = kin[used_ids.cuda()].cpu()
+    v_before[used_ids] = vin[used_ids.cuda()].cpu()
+    q, kn, vn = w.q.cuda(), w.k_new.cuda(), w.v_new.cuda()
+    bt, cl = w.block_tables.cuda(), w.context_lens.cuda()
+    ka, va = kin.clone(), vin.clone()
+    binding.write_cache_fp8(kn, vn, w.slot_mapping.cuda(), ka, va, k_scale, v_scale)
+    out_a = binding.decode_fp8(q, ka, va, bt, cl, w.scale, k_scale, v_scale)
+    out_b = binding.decode_fp8_append(q, kn, vn, kin, vin, bt, cl, w.scale, k_scale, v_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out_b.view(torch.int16), out_a.view(torch.int16))
+    assert torch.equal(kin, ka) and torch.equal(vin, va)
+    del ka, va
+    # The newest tokens' codes, against the oracle's quantiser.
+    for s in sample:
+        slot = int(w.slot_mapping[s])
+        assert np.array_equal(kin[slot // bs, slot % bs].cpu().numpy(), ofp8.quantize(w.k_new[s].float().numpy(), k_scale))
+        assert np.array_equal(vin[slot // bs, slot % bs].cpu().numpy(), ofp8.quantize(w.v_new[s].float().numpy(), v_scale))
+    kc, bt2, ctx2, slots = _compact(w, k_before, sample)
+    vc, _, _, _ = _compact(w, v_before, sample)
+    k_ref, v_ref = ofp8.write_cache_fp8(kc, vc, w.k_new[sample].float().numpy(), w.v_new[sample].float().numpy(),
+                                        slots, bs, k_scale, v_scale)
+    want = ofp8.decode_fp8(w.q[sample].double().numpy(), k_ref, v_ref, bt2, ctx2, w.scale, bs, k_scale, v_scale)
+    assert_close(out_b[sample], want, "bf16", f"fp8 full {name}")
+    assert torch.isfinite(out_b).all()

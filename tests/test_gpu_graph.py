@@ -1,6 +1,7 @@
-"""The decode step (cache write + pa_decode_ws) captured into a CUDA graph:
-replays give the same result as eager calls and as the oracle.  pa_decode_ws
-allocates nothing and never synchronises, so it can be captured."""
+"""The decode step captured into a CUDA graph, in both launch forms (cache
+write + pa_decode_ws, and the fused pa_decode_append with caller scratch):
+replays give the same result as eager calls and as the oracle.  With caller
+scratch neither allocates nor synchronises, so both can be captured."""
 
 import pytest
 import torch
@@ -58,3 +59,39 @@ def test_captured_step_matches_eager_and_oracle(name):
     assert torch.equal(out, eager)
     k_ref, v_ref = oracle_pools_after_write(w)
     assert_close(out, oracle_decode(w, k_ref, v_ref), sp.dtype, f"graph {name}")
+
+
+def test_captured_fused_step_matches_eager_and_oracle():
+    """The step the benchmark times, pa_decode_append with caller scratch,
+    captured once and replayed: each replay writes the newest tokens again
+    (the same bytes) and decodes."""
+    sp = workloads.spec("llama3_8b", num_seqs=12, ctx_lo=1, ctx_hi=700, max_context=704, pool_blocks=600)
+    w = workloads.make_workload(sp, prewritten=False, poison=True)
+    g = to_device(w)
+    S, H, D = w.q.shape
+    need = binding.pa_decode_workspace_size(S, H, sp.num_kv_heads, D)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    out = torch.zeros_like(g["q"])
+
+    def step():
+        binding.decode_append(g["q"], g["k_new"], g["v_new"], g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], w.scale, out=out, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    out.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    k_ref, v_ref = oracle_pools_after_write(w)
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), k_ref.view(torch.int16))
+    assert_close(out, oracle_decode(w, k_ref, v_ref), "bf16", "graph fused step")
