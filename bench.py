@@ -56,19 +56,27 @@ WORKLOADS = {
 }
 
 
-def step_bytes(w) -> dict:
-    """Algorithmic bytes of one step (nothing that a perfect kernel could avoid)."""
+def step_bytes(w, queries: int = 1, kv_fp8: bool = False) -> dict:
+    """Algorithmic bytes of one step (nothing that a perfect kernel could avoid):
+    the decode reads K+V over the valid contexts (one byte per element for FP8
+    pools), the queries, the valid block-table entries and the lengths, and
+    writes the outputs; the cache write reads each new token's K/V rows and
+    stores them (quantised for FP8 pools) with an int64 slot per token.
+    `queries` new tokens per sequence sit at positions c - Q .. c - 1; those at
+    negative positions are not written."""
     sp = w.spec
     e = 4 if sp.dtype == "f32" else 2
+    pe = 1 if kv_fp8 else e
+    Q = queries
     ctx = w.context_lens.numpy().astype(np.int64)
     nblk = -(-ctx // sp.block_size)
-    kv = int(ctx.sum()) * 2 * sp.num_kv_heads * sp.head_size * e
-    qo = 2 * sp.num_seqs * sp.num_heads * sp.head_size * e
+    kv = int(ctx.sum()) * 2 * sp.num_kv_heads * sp.head_size * pe
+    qo = 2 * sp.num_seqs * Q * sp.num_heads * sp.head_size * e
     tables = 4 * int(nblk.sum()) + 4 * sp.num_seqs
     decode = kv + qo + tables
-    wr_tokens = int((w.slot_mapping.numpy() >= 0).sum())
-    write = 2 * 2 * wr_tokens * sp.num_kv_heads * sp.head_size * e + 8 * sp.num_seqs
-    # Unique physical K/V actually resident (prefix blocks counted once).
+    wr_tokens = int(np.minimum(ctx, Q).sum()) if Q > 1 else int((w.slot_mapping.numpy() >= 0).sum())
+    row = sp.num_kv_heads * sp.head_size
+    write = wr_tokens * 2 * row * (e + pe) + 8 * sp.num_seqs * Q
     return {"decode": decode, "write": write, "step": decode + write, "kv_logical": kv}
 
 
@@ -345,13 +353,16 @@ def measure(args, lib, dev, world, rank, local, cpu_baseline=True):
 
     w = make_replica(args.workload, rank, args.block_size)
     sp = w.spec
-    by = step_bytes(w)
+    Q = args.queries
+    fp8 = args.kv == "fp8"
+    if fp8 and sp.dtype != "bf16":
+        raise SystemExit("--kv fp8 needs a bf16 workload (bf16 queries and new rows)")
+    by = step_bytes(w, Q, fp8)
     S, H, D = w.q.shape
     Hk, bs, NB, MB = sp.num_kv_heads, sp.block_size, w.num_blocks, w.max_blocks_per_seq
     dt = binding.dtype_code(w.q.dtype)
     g = {k: getattr(w, k).to(dev) for k in ("q", "k_cache", "v_cache", "block_tables", "context_lens",
                                              "slot_mapping", "k_new", "v_new")}
-    Q = args.queries
     if Q > 1:
         # Several new tokens per sequence (positions c-Q .. c-1): their query
         # rows, their K/V rows and their slots; the pool already holds them.
@@ -365,23 +376,11 @@ def measure(args, lib, dev, world, rank, local, cpu_baseline=True):
                 pos = c - Q + i
                 slots.append(-1 if pos < 0 else int(w.block_tables[s_, pos // bs]) * bs + pos % bs)
         g["slot_mapping"] = torch.tensor(slots, dtype=torch.int64, device=dev)
-        e_ = 2 if sp.dtype == "bf16" else 4
-        extra = (Q - 1) * S * (2 * H * D * e_ + 2 * 2 * Hk * D * e_ + 8)
-        by = dict(by, decode=by["decode"] + (Q - 1) * 2 * S * H * D * e_)
-        by["step"] += extra
-    fp8 = args.kv == "fp8"
     if fp8:
-        if Q > 1 or sp.dtype != "bf16":
-            raise SystemExit("--kv fp8 needs bf16 and one query per sequence")
         # E4M3 pools (one scale per pool); the prompt's K/V quantised once here.
         k_scale = v_scale = 1.0
         g["k_cache"] = (g["k_cache"].float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
         g["v_cache"] = (g["v_cache"].float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
-        e_kv = Hk * D * 2  # per token: K+V bytes saved by one-byte elements
-        ctx_tok = int(w.context_lens.sum())
-        by = dict(by, decode=by["decode"] - ctx_tok * e_kv, kv_logical=by["kv_logical"] // 2)
-        by["write"] -= S * 2 * Hk * D  # the write stores one byte per element instead of two
-        by["step"] = by["decode"] + by["write"]
     n_new = S * Q
     out = torch.empty_like(g["q"])
     stream = torch.cuda.current_stream(dev)
@@ -413,7 +412,12 @@ def measure(args, lib, dev, world, rank, local, cpu_baseline=True):
             raise RuntimeError(binding.pa_last_error())
 
     def decode(gg, o, sh=sh):
-        if fused and fp8:
+        if fused and fp8 and Q > 1:
+            rc = lib.pa_decode_fp8_mq_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
+                                             P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, Q, H,
+                                             Hk, D, bs, MB, w.scale, k_scale, v_scale, sh, 0, P(ws), ws_bytes, 0,
+                                             None)
+        elif fused and fp8:
             rc = lib.pa_decode_fp8_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
                                           P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, H, Hk, D,
                                           bs, MB, w.scale, k_scale, v_scale, sh, 0, P(ws), ws_bytes, 0, None)
@@ -425,6 +429,10 @@ def measure(args, lib, dev, world, rank, local, cpu_baseline=True):
             rc = lib.pa_decode_append(P(o), P(gg["q"]), P(gg["k_new"]), P(gg["v_new"]), P(g["k_cache"]),
                                       P(g["v_cache"]), P(gg["block_tables"]), P(gg["context_lens"]), S, H, Hk, D,
                                       bs, MB, w.scale, sh, dt, 0, P(ws), ws_bytes, 0, None)
+        elif fp8 and Q > 1:
+            rc = lib.pa_decode_fp8_mq(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
+                                      P(gg["context_lens"]), S, Q, H, Hk, D, bs, MB, w.scale, k_scale, v_scale, sh,
+                                      0, P(ws), ws_bytes, 0, None)
         elif fp8:
             rc = lib.pa_decode_fp8(P(o), P(gg["q"]), P(g["k_cache"]), P(g["v_cache"]), P(gg["block_tables"]),
                                    P(gg["context_lens"]), S, H, Hk, D, bs, MB, w.scale, k_scale, v_scale, sh, 0,
@@ -600,7 +608,8 @@ def measure(args, lib, dev, world, rank, local, cpu_baseline=True):
             "step_bytes": by["step"], "decode_bytes": by["decode"], "write_bytes": by["write"],
             "unique_kv_bytes": unique_kv_bytes(w, 1 if fp8 else (2 if sp.dtype == "bf16" else 4)),
             "write_us": None if fused else wr_ms * 1e3,
-            "step": (("pa_decode_fp8_append" if fp8 else "pa_decode_mq_append" if Q > 1 else "pa_decode_append") +
+            "step": ((("pa_decode_fp8_mq_append" if Q > 1 else "pa_decode_fp8_append") if fp8
+                      else "pa_decode_mq_append" if Q > 1 else "pa_decode_append") +
                      (" (cache write fused into the decode, one launch)" if launches == 1
                       else " (row-writing kernel chained ahead of the decode, two launches)") if fused
                      else "cache write + decode (two launches)"),

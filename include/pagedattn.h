@@ -179,7 +179,7 @@ int pa_decode_append(void* out, const void* query, const void* k_new, const void
  * The num_queries newest tokens of every sequence must already be in the pool
  * (pa_write_cache) and counted in context_lens.  A query whose position is
  * negative (context shorter than num_queries) gets a zero row.
- * Requires dtype PA_BF16 and (num_heads / num_kv_heads) * num_queries <= 16;
+ * Requires dtype PA_BF16 and (num_heads / num_kv_heads) * num_queries <= 32;
  * num_queries == 1 is plain decode.  Other arguments as in pa_decode_ex; the
  * scratch size comes from pa_decode_mq_workspace_size (workspace NULL: the
  * library's own, allocated on first use).
@@ -203,8 +203,8 @@ size_t pa_decode_mq_workspace_size(int num_seqs, int num_queries, int num_heads,
  * >= 0 into the pool (block_tables[s][pos / block_size], row
  * pos % block_size) and returns the same `out` as pa_write_cache of those
  * rows followed by pa_decode_mq.  One launch instead of two when
- * (num_heads / num_kv_heads) * num_queries <= 8; above that (two consumer
- * warps per KV head) the call launches a row-writing kernel and then the
+ * (num_heads / num_kv_heads) * num_queries <= 8; above that (two to four
+ * consumer warps per KV head) the call launches a row-writing kernel and then the
  * decode on `stream`, chained by programmatic dependent launch.
  * k_new, v_new  [num_seqs * num_queries, num_kv_heads, head_size], bf16,
  *               16-byte aligned
@@ -285,7 +285,8 @@ int pa_decode_static(void* out, const void* query, const void* k_cache, const vo
  * k_cache/v_cache are uint8 [num_physical_blocks, block_size, num_kv_heads,
  * head_size].  error_flag as in pa_write_cache_ex (optional).
  *
- * pa_decode_fp8 - pa_decode_ex over FP8 pools, query and out bf16: scores use
+ * pa_decode_fp8 - pa_decode_ex over FP8 pools (one query per sequence; several:
+ * pa_decode_fp8_mq), query and out bf16: scores use
  * k = e4m3(code) * k_scale and values v = e4m3(code) * v_scale.  Each token
  * moves half the bytes of a bf16 pool.  Scratch as pa_decode_workspace_size.
  * The query is rounded to f16 on the way into the tensor cores (exact for
@@ -316,6 +317,40 @@ int pa_decode_fp8_append(void* out, const void* query, const void* k_new, const 
                          int head_size, int block_size, int max_blocks_per_seq, float scale,
                          float k_scale, float v_scale, void* stream, int num_physical_blocks,
                          void* workspace, size_t workspace_bytes, int num_ranges, int32_t* error_flag);
+
+/*
+ * pa_decode_fp8_mq - pa_decode_mq over FP8 pools: several causal query tokens
+ * per sequence (chunked prefill, speculative-decoding verification) reading
+ * the quantised cache.  Keys and values are e4m3(code) * k_scale and
+ * e4m3(code) * v_scale as in pa_decode_fp8; query and out are bf16
+ * [num_seqs, num_queries, num_heads, head_size]; query i of sequence s sees
+ * positions 0 .. context_lens[s] - num_queries + i.  Requires
+ * (num_heads / num_kv_heads) * num_queries <= 32.  Scratch size:
+ * pa_decode_mq_workspace_size.  Other arguments and limits as in
+ * pa_decode_fp8 and pa_decode_mq.
+ *
+ * pa_decode_fp8_mq_append - the same with the step's quantising cache write
+ * fused in: k_new / v_new [num_seqs * num_queries, num_kv_heads, head_size]
+ * bf16 (row s * num_queries + i: position context_lens[s] - num_queries + i)
+ * are quantised as pa_write_cache_fp8 does (bit-identical codes) and stored
+ * into the pools; tokens at negative positions are skipped.  Up to 8
+ * (query, head) columns per KV head the decode launch itself writes them;
+ * above that a row-writing kernel is chained ahead of the decode.  out equals
+ * pa_write_cache_fp8 of those rows followed by pa_decode_fp8_mq.
+ */
+int pa_decode_fp8_mq(void* out, const void* query, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                     int num_queries, int num_heads, int num_kv_heads, int head_size, int block_size,
+                     int max_blocks_per_seq, float scale, float k_scale, float v_scale, void* stream,
+                     int num_physical_blocks, void* workspace, size_t workspace_bytes, int num_ranges,
+                     int32_t* error_flag);
+int pa_decode_fp8_mq_append(void* out, const void* query, const void* k_new, const void* v_new,
+                            void* k_cache, void* v_cache, const int32_t* block_tables,
+                            const int32_t* context_lens, int num_seqs, int num_queries, int num_heads,
+                            int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
+                            float scale, float k_scale, float v_scale, void* stream,
+                            int num_physical_blocks, void* workspace, size_t workspace_bytes,
+                            int num_ranges, int32_t* error_flag);
 
 /*
  * pa_test_stall_copy - test hook for the decode kernel's bounded waits; the

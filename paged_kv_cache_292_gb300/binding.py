@@ -80,6 +80,16 @@ _SIGS = {
         [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, ctypes.c_float, ctypes.c_float, _P, _I,
          _P, _SZ, _I, _P],
     ),
+    "pa_decode_fp8_mq": (
+        _I,
+        [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, ctypes.c_float, ctypes.c_float, _P,
+         _I, _P, _SZ, _I, _P],
+    ),
+    "pa_decode_fp8_mq_append": (
+        _I,
+        [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, ctypes.c_float,
+         ctypes.c_float, _P, _I, _P, _SZ, _I, _P],
+    ),
     "pa_decode_static": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _I]),
     "pa_write_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I]),
     "pa_write_cache_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P]),
@@ -477,4 +487,38 @@ def decode_fp8(query, k_cache, v_cache, block_tables, context_lens, scale, k_sca
                                 _ptr(context_lens), S, H, Hk, D, bs, block_tables.shape[1], float(scale),
                                 float(k_scale), float(v_scale), _stream(stream), NB if check_block_ids else 0,
                                 _ptr(workspace), ws_bytes, num_ranges, _ptr(error_flag)))
+    return out
+
+
+def decode_fp8_multi(query, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale, out=None,
+                     stream=None, *, num_ranges=0, workspace=None, error_flag=None, check_block_ids=False):
+    """out[S, Q, H, D] (bf16): several causal query tokens per sequence over uint8 E4M3 pools."""
+    _require_cuda(query, k_cache, v_cache, block_tables, context_lens, out, workspace, error_flag)
+    S, Q, H, D = query.shape
+    NB, bs, Hk, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(query)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pa_decode_fp8_mq(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                   _ptr(context_lens), S, Q, H, Hk, D, bs, block_tables.shape[1], float(scale),
+                                   float(k_scale), float(v_scale), _stream(stream), NB if check_block_ids else 0,
+                                   _ptr(workspace), ws_bytes, num_ranges, _ptr(error_flag)))
+    return out
+
+
+def decode_fp8_multi_append(query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, k_scale,
+                            v_scale, out=None, stream=None, *, num_ranges=0, workspace=None, error_flag=None,
+                            check_block_ids=False):
+    """pa_decode_fp8_mq_append: the FP8 multi-query step with the Q new rows' quantising write fused in."""
+    _require_cuda(query, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, workspace, error_flag)
+    S, Q, H, D = query.shape
+    NB, bs, Hk, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(query)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pa_decode_fp8_mq_append(_ptr(out), _ptr(query), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                          _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), S, Q, H, Hk, D, bs,
+                                          block_tables.shape[1], float(scale), float(k_scale), float(v_scale),
+                                          _stream(stream), NB if check_block_ids else 0, _ptr(workspace), ws_bytes,
+                                          num_ranges, _ptr(error_flag)))
     return out

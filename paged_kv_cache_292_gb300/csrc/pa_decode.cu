@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstring>
 #include <type_traits>
 
 #include "../../include/pagedattn.h"
@@ -57,9 +58,9 @@ int heads_per_cta(int num_kv_heads, int head_size, int elt, int max_heads = kMax
   return 1;
 }
 
-// Consumer warps per KV head: two when a KV head has more than 8 (query, head)
-// columns (one 8-wide MMA tile per warp), else one.
-int column_split(int group, int num_queries) { return group * num_queries > 8 ? 2 : 1; }
+// Consumer warps per KV head: one 8-wide MMA tile of (query, head) columns
+// per warp, so ceil(columns / 8) (at most 4: 32 columns).
+int column_split(int group, int num_queries) { return (group * num_queries + 7) / 8; }
 
 int default_ranges(const DeviceInfo& dev, int HG) {
   const int r = dev.sm_count / HG;
@@ -204,6 +205,22 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
+// Encoded maps of the last few pools this thread decoded over.  A map is a
+// pure function of the pool's address, extents, strides and box, which form
+// the key, so a hit is exactly what a fresh encode would give; repeated
+// steps over the same pools skip the driver call.
+struct TensorMapCacheEntry {
+  const void* k;
+  const void* v;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  CUtensorMap tm_k, tm_v;
+  bool used;
+};
+constexpr int kTensorMapCache = 4;
+thread_local TensorMapCacheEntry g_tmap_cache[kTensorMapCache];
+thread_local int g_tmap_next = 0;
+
 int make_tensor_maps(DecodeParams* prm, const Plan& pl, int num_kv_heads, int head_size, int kv_elt,
                      int block_size, int num_physical_blocks) {
   const EncodeTiledFn enc = encode_tiled_fn();
@@ -220,6 +237,15 @@ int make_tensor_maps(DecodeParams* prm, const Plan& pl, int num_kv_heads, int he
                                  (cuuint64_t)num_kv_heads * head_size * kv_elt};
   const cuuint32_t box[4] = {kLine, pl.lines, 1u, pl.box_rows};
   const cuuint32_t estride[4] = {1u, 1u, 1u, 1u};
+  for (int c = 0; c < kTensorMapCache; ++c) {
+    const TensorMapCacheEntry& e = g_tmap_cache[c];
+    if (e.used && e.k == prm->k_cache && e.v == prm->v_cache && memcmp(e.dims, dims, sizeof(dims)) == 0 &&
+        memcmp(e.strides, strides, sizeof(strides)) == 0 && memcmp(e.box, box, sizeof(box)) == 0) {
+      prm->tm_k = e.tm_k;
+      prm->tm_v = e.tm_v;
+      return PA_OK;
+    }
+  }
   for (int i = 0; i < 2; ++i) {
     const CUresult r = enc(i ? &prm->tm_v : &prm->tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
                            const_cast<void*>(i ? prm->v_cache : prm->k_cache), dims, strides, box,
@@ -228,6 +254,16 @@ int make_tensor_maps(DecodeParams* prm, const Plan& pl, int num_kv_heads, int he
     if (r != CUDA_SUCCESS)
       return fail(PA_ERR_CUDA, "pa_decode: cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
   }
+  TensorMapCacheEntry& e = g_tmap_cache[g_tmap_next];
+  g_tmap_next = (g_tmap_next + 1) % kTensorMapCache;
+  e.k = prm->k_cache;
+  e.v = prm->v_cache;
+  memcpy(e.dims, dims, sizeof(dims));
+  memcpy(e.strides, strides, sizeof(strides));
+  memcpy(e.box, box, sizeof(box));
+  e.tm_k = prm->tm_k;
+  e.tm_v = prm->tm_v;
+  e.used = true;
   return PA_OK;
 }
 
@@ -257,7 +293,11 @@ template <typename T, int D>
 int launch_dtype(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t stream,
                  bool kv_fp8 = false) {
   if constexpr (sizeof(T) == 2) {
-    if (kv_fp8) return launch_typed<T, D, 8, 0, true>(prm, pl, dev, stream);
+    if (kv_fp8) {
+      if (prm.num_queries == 1) return launch_typed<T, D, 8, 0, true>(prm, pl, dev, stream);
+      return prm.group * prm.num_queries <= 8 ? launch_typed<T, D, 8, 1, true>(prm, pl, dev, stream)
+                                               : launch_typed<T, D, 8, 2, true>(prm, pl, dev, stream);
+    }
     if (prm.num_queries > 1)  // (query, head) columns in one or two 8-wide MMA tiles
       return prm.group * prm.num_queries <= 8 ? launch_typed<T, D, 8, 1>(prm, pl, dev, stream)
                                                : launch_typed<T, D, 8, 2>(prm, pl, dev, stream);
@@ -291,14 +331,11 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
     if (k_new == nullptr || v_new == nullptr)
       return fail(PA_ERR_INVALID_ARG, "pa_decode_append: k_new and v_new are both needed");
     if (dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_decode_append: bf16 queries and pools only");
-    if (kv_fp8 && num_queries != 1)
-      return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8_append: one query per sequence");
     if (!aligned(k_new, 16) || !aligned(v_new, 16))
       return fail(PA_ERR_INVALID_ARG, "pa_decode_append: k_new / v_new not 16-byte aligned");
   }
   if (kv_fp8) {
     if (dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: query/out must be bf16");
-    if (num_queries != 1) return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: one query per sequence");
     if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale <= 0.f || v_scale <= 0.f)
       return fail(PA_ERR_INVALID_ARG, "pa_decode_fp8: scales must be finite and positive");
   }
@@ -309,9 +346,9 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   if (num_queries < 1) return fail(PA_ERR_INVALID_ARG, "pa_decode_mq: num_queries %d < 1", num_queries);
   if (num_queries > 1 && dtype != PA_BF16)
     return fail(PA_ERR_UNSUPPORTED, "pa_decode_mq: several queries need bf16");
-  if (num_queries > 1 && (num_heads / num_kv_heads) * num_queries > 16)
-    return fail(PA_ERR_UNSUPPORTED, "pa_decode_mq: group size x queries = %d > 16",
-                (num_heads / num_kv_heads) * num_queries);
+  if (num_queries > 1 && (num_heads / num_kv_heads) * num_queries > kMaxColumns)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_mq: group size x queries = %d > %d",
+                (num_heads / num_kv_heads) * num_queries, kMaxColumns);
   DeviceInfo dev{};
   rc = current_device_info(&dev);
   if (rc != PA_OK) return rc;
@@ -365,6 +402,7 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   prm.num_physical_blocks = num_physical_blocks;
   prm.stages = pl.stages;
   prm.num_queries = num_queries;
+  prm.split = pl.split;
   prm.q_slots = pl.q_slots;
   prm.row_bytes = pl.row_bytes;
   prm.pitch = pl.pitch;
@@ -390,12 +428,13 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(merge tickets)");
   }
   take_wait_test(&prm.stall_tile, &prm.wait_limit_ns);
-  if (k_new != nullptr && pl.split == 2) {
+  if (k_new != nullptr && pl.split >= 2) {
     // Two consumer warps per KV head: the rows are written by their own
     // kernel, chained ahead of the decode, which then only reads them.
     rc = append_rows_impl(k_new, v_new, block_tables, context_lens, const_cast<void*>(k_cache),
                           const_cast<void*>(v_cache), num_seqs, num_queries, num_kv_heads, head_size,
-                          block_size, max_blocks_per_seq, num_physical_blocks, stream, error_flag);
+                          block_size, max_blocks_per_seq, num_physical_blocks, stream, error_flag,
+                          kv_fp8, k_scale, v_scale);
     if (rc != PA_OK) return rc;
     prm.k_new = prm.v_new = nullptr;
   }
@@ -563,4 +602,33 @@ extern "C" int pa_decode_fp8(void* out, const void* query, const void* k_cache, 
                            num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, scale,
                            stream, PA_BF16, num_physical_blocks, workspace, workspace_bytes,
                            num_ranges, error_flag, true, k_scale, v_scale);
+}
+
+extern "C" int pa_decode_fp8_mq(void* out, const void* query, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                int num_queries, int num_heads, int num_kv_heads, int head_size,
+                                int block_size, int max_blocks_per_seq, float scale, float k_scale,
+                                float v_scale, void* stream, int num_physical_blocks, void* workspace,
+                                size_t workspace_bytes, int num_ranges, int32_t* error_flag) {
+  return pa::decode_impl_q(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                           num_queries, num_heads, num_kv_heads, head_size, block_size,
+                           max_blocks_per_seq, scale, stream, PA_BF16, num_physical_blocks, workspace,
+                           workspace_bytes, num_ranges, error_flag, true, k_scale, v_scale);
+}
+
+extern "C" int pa_decode_fp8_mq_append(void* out, const void* query, const void* k_new, const void* v_new,
+                                       void* k_cache, void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, int num_seqs, int num_queries,
+                                       int num_heads, int num_kv_heads, int head_size, int block_size,
+                                       int max_blocks_per_seq, float scale, float k_scale, float v_scale,
+                                       void* stream, int num_physical_blocks, void* workspace,
+                                       size_t workspace_bytes, int num_ranges, int32_t* error_flag) {
+  if (k_new == nullptr || v_new == nullptr) {
+    pa::clear_error();
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_decode_fp8_mq_append: null k_new / v_new");
+  }
+  return pa::decode_impl_q(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                           num_queries, num_heads, num_kv_heads, head_size, block_size,
+                           max_blocks_per_seq, scale, stream, PA_BF16, num_physical_blocks, workspace,
+                           workspace_bytes, num_ranges, error_flag, true, k_scale, v_scale, k_new, v_new);
 }

@@ -24,8 +24,8 @@
 //     bulk copy per token row, rows `row + 16` bytes apart.  Each sequence's
 //     query slice is copied once into a small ring of its own.
 //   * Each consumer warp owns one KV head and its G query heads (with several
-//     query tokens and more than 8 (query, head) columns, two warps share a KV
-//     head, 8 columns each).  bf16: S^T[16 tok x 8] = K_tile[16 x D] *
+//     query tokens and more than 8 (query, head) columns, two to four warps
+//     share a KV head, 8 columns each).  bf16: S^T[16 tok x 8] = K_tile[16 x D] *
 //     Q^T[D x 8] on the tensor cores (mma.sync m16n8k16, query heads padded
 //     to 8), online softmax in registers (running max and sum in the exp2
 //     domain), then O^T[D x 8] += V^T[D x 16] * P^T[16 x 8], with P^T obtained
@@ -62,6 +62,7 @@ namespace pa {
 
 constexpr int kMaxGroupHeads = 8;  // KV heads per CTA (one consumer warp each)
 constexpr int kMaxQueryGroup = 8;  // query heads per KV head (MMA N extent)
+constexpr int kMaxColumns = 32;    // (query, head) columns per KV head: four consumer warps of 8
 constexpr int kRowSkew = 16;       // fp32 stages: bytes between staged rows beyond the row itself
 constexpr uint32_t kLine = 128;    // tensor-core stages: bytes per swizzled line
 constexpr int kMaxRowBytes = 2048;  // bytes of one staged token row (K or V)
@@ -106,6 +107,7 @@ struct DecodeParams {
   int num_physical_blocks;
   int stages, q_slots;
   int num_queries;  // query tokens per sequence (1 for plain decode)
+  int split;        // consumer warps per KV head: ceil(G * num_queries / 8), 8 columns each
   float v_scale;    // FP8 pools: value of a V code is decode(code) * v_scale (else 1)
   float k_scale;    // FP8 pools: value of a K code is decode(code) * k_scale (else 1)
   uint32_t row_bytes, pitch, q_bytes, stage_bytes;
@@ -573,27 +575,44 @@ struct MmaConsumerMQ {
 // Scores carry k_scale in scale_log2; v_scale is applied to the output.  The
 // bf16 query converts to f16 exactly for |q| in f16's normal range
 // [2^-14, 65504]; P enters as f16.
-template <int D>
+// MQ: several query tokens per sequence with a causal mask, as in
+// MmaConsumerMQ: column n = col0 + (lane / 4) holds (query n / G, head n % G),
+// query qi sits at position ctx - Q + qi and sees tokens up to it.
+template <int D, bool MQ = false>
 struct MmaConsumerF8 {
   static constexpr int KS = D / 16;
   uint32_t qb[KS][2];
   float acc[KS][4];
   float m_a, m_b, l_a, l_b;
   uint32_t lane_off = 0;  // this lane's ldmatrix row address within a half-stage (K and V alike)
+  int col0 = 0;           // MQ: first (query, head) column of this warp
 
   // Once per kernel: uh is the head's first 16-byte unit in the group's row.
   __device__ __forceinline__ void setup(uint32_t lines, int uh, int lane) {
     lane_off = RowPtr<1>(0u, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines).a[0];
   }
 
-  __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G,
-                                                int lane) {
-    const int n = lane >> 2, t4 = 4 * (lane & 3);
-    const __nv_bfloat16* qh =
-        reinterpret_cast<const __nv_bfloat16*>(qslot) + (size_t)(w * G + n) * D;
+  // w: KV head within the CTA's group.  MQ also takes Q, Hg and this warp's
+  // first column.
+  __device__ __forceinline__ void begin_segment(const unsigned char* qslot, int w, int G, int lane,
+                                                int Q = 1, int Hg = 1, int col_base = 0) {
+    const int t4 = 4 * (lane & 3);
+    const __nv_bfloat16* qh;
+    bool real;
+    if constexpr (MQ) {
+      col0 = col_base;
+      const int n = col_base + (lane >> 2);
+      real = n < G * Q;
+      const int qi = real ? n / G : 0, g = real ? n % G : 0;
+      qh = reinterpret_cast<const __nv_bfloat16*>(qslot) + ((size_t)qi * Hg * G + w * G + g) * D;
+    } else {
+      const int n = lane >> 2;
+      real = n < G;
+      qh = reinterpret_cast<const __nv_bfloat16*>(qslot) + (size_t)(w * G + n) * D;
+    }
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      if (n < G) {
+      if (real) {
         const uint2 v = *reinterpret_cast<const uint2*>(qh + ks * 16 + t4);  // dims t4 .. t4+3
         qb[ks][0] = pack_f16x2(bf16_lo(v.x), bf16_hi(v.x));  // k pair (2t, 2t+1)
         qb[ks][1] = pack_f16x2(bf16_lo(v.y), bf16_hi(v.y));  // k pair (2t+8, 2t+9)
@@ -608,8 +627,9 @@ struct MmaConsumerF8 {
     l_a = l_b = 0.f;
   }
 
+  // MQ: tok0 (first token of the tile), ctx, G and Q give the causal limits.
   __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, int nvalid, float scale_log2,
-                                       int lane) {
+                                       int lane, int tok0 = 0, int ctx = 0, int G = 1, int Q = 1) {
     // Matrices of one ldmatrix.x4: (rows 0-7, bytes 0-15), (rows 8-15, 0-15),
     // (rows 0-7, 16-31), (rows 8-15, 16-31) - two k-steps / m-tiles of 16 dims.
     // Half-stages are 1 KiB aligned, so adding the lane offset keeps the
@@ -638,6 +658,17 @@ struct MmaConsumerF8 {
     float s2 = (c0[2] + c1[2]) * scale_log2, s3 = (c0[3] + c1[3]) * scale_log2;
     if (g >= nvalid) s0 = s1 = -INFINITY;
     if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
+    if constexpr (MQ) {
+      // Last visible position of each column's query (-1: padding column).
+      const int na = col0 + t2, nb = na + 1;
+      const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
+      const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
+      const int t0 = tok0 + g, t1 = t0 + 8;
+      if (t0 > lim_a) s0 = -INFINITY;
+      if (t0 > lim_b) s1 = -INFINITY;
+      if (t1 > lim_a) s2 = -INFINITY;
+      if (t1 > lim_b) s3 = -INFINITY;
+    }
     float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -696,7 +727,9 @@ struct MmaConsumerF8 {
     }
   }
 
-  // Output row pairs: acc[mt][0] / [2] are dims dd / dd+1 of head hA, [1] / [3] of hB.
+  // Output row pairs: acc[mt][0] / [2] are dims dd / dd+1 of column a,
+  // [1] / [3] of column b.  Output rows are [seq][query][head]; partial rows
+  // are [query][head] (one query: [head]).
   __device__ __forceinline__ void finish(const DecodeParams& p, int seq, int kv_head, int slot,
                                          int r, int lane) {
     float la = l_a, lb = l_b;
@@ -705,39 +738,65 @@ struct MmaConsumerF8 {
       la += __shfl_xor_sync(0xffffffffu, la, o);
       lb += __shfl_xor_sync(0xffffffffu, lb, o);
     }
-    const int G = p.group, H = p.num_heads;
-    const int ha = 2 * (lane & 3), hb = ha + 1, g = lane >> 2;
-    const int qa = kv_head * G + ha, qb_ = kv_head * G + hb;
-    if (slot < 0) {
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)seq * H * D;
-      const float ia = p.v_scale / la, ib = p.v_scale / lb;
+    const int G = p.group, H = p.num_heads, Q = MQ ? p.num_queries : 1;
+    const int g = lane >> 2;
+    if constexpr (!MQ) {
+      const int ha = 2 * (lane & 3), hb = ha + 1;
+      const int qa = kv_head * G + ha, qb_ = kv_head * G + hb;
+      if (slot < 0) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)seq * H * D;
+        const float ia = p.v_scale / la, ib = p.v_scale / lb;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        const int dd = mt * 16 + 2 * g;
-        if (ha < G)
-          *reinterpret_cast<uint32_t*>(out + (size_t)qa * D + dd) = pack_bf16x2(acc[mt][0] * ia, acc[mt][2] * ia);
-        if (hb < G)
-          *reinterpret_cast<uint32_t*>(out + (size_t)qb_ * D + dd) = pack_bf16x2(acc[mt][1] * ib, acc[mt][3] * ib);
-      }
-    } else {
-      const size_t base = ((size_t)r * 2 + slot) * H;
-      float* po = p.part_o + base * D;
+        for (int mt = 0; mt < KS; ++mt) {
+          const int dd = mt * 16 + 2 * g;
+          if (ha < G)
+            *reinterpret_cast<uint32_t*>(out + (size_t)qa * D + dd) = pack_bf16x2(acc[mt][0] * ia, acc[mt][2] * ia);
+          if (hb < G)
+            *reinterpret_cast<uint32_t*>(out + (size_t)qb_ * D + dd) = pack_bf16x2(acc[mt][1] * ib, acc[mt][3] * ib);
+        }
+      } else {
+        const size_t base = ((size_t)r * 2 + slot) * H;
+        float* po = p.part_o + base * D;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        const int dd = mt * 16 + 2 * g;
-        if (ha < G) *reinterpret_cast<float2*>(po + (size_t)qa * D + dd) = make_float2(acc[mt][0], acc[mt][2]);
-        if (hb < G) *reinterpret_cast<float2*>(po + (size_t)qb_ * D + dd) = make_float2(acc[mt][1], acc[mt][3]);
+        for (int mt = 0; mt < KS; ++mt) {
+          const int dd = mt * 16 + 2 * g;
+          if (ha < G) *reinterpret_cast<float2*>(po + (size_t)qa * D + dd) = make_float2(acc[mt][0], acc[mt][2]);
+          if (hb < G) *reinterpret_cast<float2*>(po + (size_t)qb_ * D + dd) = make_float2(acc[mt][1], acc[mt][3]);
+        }
+        if (g == 0) {
+          float* pm = p.part_ml + base * 2;
+          if (ha < G) *reinterpret_cast<float2*>(pm + (size_t)qa * 2) = make_float2(m_a, la);
+          if (hb < G) *reinterpret_cast<float2*>(pm + (size_t)qb_ * 2) = make_float2(m_b, lb);
+        }
       }
-      if (g == 0) {
-        float* pm = p.part_ml + base * 2;
-        if (ha < G) {
-          pm[(size_t)qa * 2 + 0] = m_a;
-          pm[(size_t)qa * 2 + 1] = la;
-        }
-        if (hb < G) {
-          pm[(size_t)qb_ * 2 + 0] = m_b;
-          pm[(size_t)qb_ * 2 + 1] = lb;
-        }
+      return;
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int n = col0 + 2 * (lane & 3) + half;
+      if (n >= G * Q) continue;
+      int qi = 0, gh = n;
+      if constexpr (MQ) {
+        qi = n / G;
+        gh = n % G;
+      }
+      const int row = qi * H + kv_head * G + gh;
+      const float l = half ? lb : la, m = half ? m_b : m_a;
+      if (slot < 0) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)seq * Q * H + row) * D;
+        // A query with no keys (several queries, short context) gives zeros.
+        const float inv = (!MQ || l > 0.f) ? p.v_scale / l : 0.f;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+          *reinterpret_cast<uint32_t*>(out + mt * 16 + 2 * g) =
+              pack_bf16x2(acc[mt][half] * inv, acc[mt][2 + half] * inv);
+      } else {
+        const size_t base = ((size_t)r * 2 + slot) * Q * H + row;
+        float* po = p.part_o + base * D;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+          *reinterpret_cast<float2*>(po + mt * 16 + 2 * g) = make_float2(acc[mt][half], acc[mt][2 + half]);
+        if (g == 0) *reinterpret_cast<float2*>(p.part_ml + base * 2) = make_float2(m, l);
       }
     }
   }
@@ -1081,7 +1140,8 @@ __device__ __forceinline__ void append_new_rows_fp8(const DecodeParams& p, const
 // ---------------------------------------------------------------------------
 // QMODE 0: one query per sequence.  QMODE 1 / 2: several query tokens per
 // sequence with a causal mask, (query, head) columns in one 8-wide MMA N-tile
-// per warp: one warp per KV head (up to 8 columns) or two (up to 16).
+// per warp: one warp per KV head (up to 8 columns) or p.split warps (2 to 4,
+// up to 32 columns).
 template <typename T, int D, int GMAX, int QMODE, bool KV8 = false>
 __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     pa_decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -1091,8 +1151,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   const int HG = p.num_head_groups, R = p.num_ranges, S = p.num_seqs;
   const int r = blockIdx.x / HG, hg = blockIdx.x % HG;
   const int Hg = p.heads_per_cta;
-  // QMODE 2 splits each KV head's 16 (query, head) columns over two warps.
-  constexpr int kSplit = QMODE == 2 ? 2 : 1;
+  // QMODE 2 splits each KV head's (query, head) columns over p.split warps,
+  // 8 columns each (up to 32 columns: four warps).
+  const int kSplit = QMODE == 2 ? p.split : 1;
   const int NCW = Hg * kSplit;  // consumer warps; warp NCW is the producer
   constexpr bool kMmaPath = (sizeof(T) == 2);  // tensor-core consumers, swizzled stages
   const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes, kMmaPath);
@@ -1355,7 +1416,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     uint32_t ph = 0, qph = 0;
     constexpr bool kMma = (sizeof(T) == 2);
     using Mma = typename std::conditional<
-        KV8, MmaConsumerF8<D>,
+        KV8, MmaConsumerF8<D, (QMODE > 0)>,
         typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, 1>>::type>::type;
     typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
     if constexpr (KV8) cons.setup(p.lines, w * D / 16, lane);
@@ -1370,8 +1431,10 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
           timed_out();
           break;
         }
-        if constexpr (QMODE == 0 || KV8)
+        if constexpr (QMODE == 0)
           cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, lane);
+        else if constexpr (KV8)
+          cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, lane, p.num_queries, Hg, col_base);
         else
           cons.begin_segment(smem + L.qring + qi * q_slot_bytes, w, G, p.num_queries, Hg, lane,
                              col_base);
@@ -1395,7 +1458,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
             append_new_rows<D>(p, mt, rows, kv_head, w, k_half, v_half, lane);
         }
       }
-      if constexpr (KV8) {
+      if constexpr (KV8 && QMODE > 0) {
+        cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane, mt.tok0, mt.ctx, G, p.num_queries);
+      } else if constexpr (KV8) {
         cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane);
       } else if constexpr (kMma && QMODE > 0) {
         cons.tile(k_half, v_half, p.lines, uh, mt.nvalid, mt.tok0, mt.ctx, G, p.num_queries,

@@ -33,11 +33,14 @@ int library_counters(size_t bytes, int32_t** ptr);
 
 // Writes the new rows of a multi-query appending call into the pools (token
 // i of sequence s at position context_lens[s] - num_queries + i), as its own
-// kernel launch on `stream`.  bf16 only; the caller validates the arguments.
+// kernel launch on `stream`.  bf16 rows; kv_fp8: quantised into FP8 pools as
+// pa_write_cache_fp8 does (k_scale, v_scale).  The caller validates the
+// arguments.
 int append_rows_impl(const void* k_new, const void* v_new, const int32_t* block_tables,
                      const int32_t* context_lens, void* k_cache, void* v_cache, int num_seqs,
                      int num_queries, int num_kv_heads, int head_size, int block_size,
-                     int max_blocks_per_seq, int num_physical_blocks, void* stream, int32_t* error_flag);
+                     int max_blocks_per_seq, int num_physical_blocks, void* stream, int32_t* error_flag,
+                     bool kv_fp8 = false, float k_scale = 1.f, float v_scale = 1.f);
 
 // The settings of pa_test_stall_copy for the decode launch about to be made on
 // this thread (then cleared): the tile whose copies are withheld (-1: none)

@@ -95,11 +95,16 @@ int write_cache_impl(const void* k_new, const void* v_new, const int64_t* slot_m
 // outside [0, max_blocks_per_seq * block_size] are clamped as the decode
 // clamps them, and a failed block-id check (num_physical_blocks > 0) leaves
 // the token unwritten and sets PA_DEVERR_BLOCK_ID.  One CTA per token.
+// KV8: the pools are FP8 (E4M3); each bf16 element x becomes the code of the
+// fp32 quotient x / scale, saturating, with the FP8 cache write's own
+// conversion, four codes per 32-bit store.  row_units counts 16-byte units of
+// a bf16 row (8 elements each).
+template <bool KV8>
 __global__ void __launch_bounds__(128) pa_append_rows_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int32_t* __restrict__ block_tables,
-    const int32_t* __restrict__ context_lens, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-    int num_seqs, int num_queries, int block_size, int max_blocks_per_seq, int row_vecs,
-    int num_physical_blocks, int32_t* error_flag) {
+    const int32_t* __restrict__ context_lens, void* __restrict__ k_cache, void* __restrict__ v_cache,
+    int num_seqs, int num_queries, int block_size, int max_blocks_per_seq, int row_units,
+    int num_physical_blocks, float k_scale, float v_scale, int32_t* error_flag) {
   griddep_wait();
   griddep_launch_dependents();
   const long long n = (long long)num_seqs * num_queries;
@@ -115,15 +120,35 @@ __global__ void __launch_bounds__(128) pa_append_rows_kernel(
       continue;
     }
     const size_t slot = (size_t)blk * block_size + pos % block_size;
-    const uint4* ks = k_new + (size_t)i * row_vecs;
-    const uint4* vs = v_new + (size_t)i * row_vecs;
-    uint4* kd = k_cache + slot * row_vecs;
-    uint4* vd = v_cache + slot * row_vecs;
-    for (int j = threadIdx.x; j < row_vecs; j += blockDim.x) {
+    const uint4* ks = k_new + (size_t)i * row_units;
+    const uint4* vs = v_new + (size_t)i * row_units;
+    for (int j = threadIdx.x; j < row_units; j += blockDim.x) {
       const uint4 kv = __ldg(ks + j);
       const uint4 vv = __ldg(vs + j);
-      kd[j] = kv;
-      vd[j] = vv;
+      if constexpr (KV8) {
+        // 8 bf16 elements -> 8 codes (two 32-bit words) per pool.
+        const uint4 src[2] = {kv, vv};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float sc = h ? v_scale : k_scale;
+          const uint32_t w[4] = {src[h].x, src[h].y, src[h].z, src[h].w};
+          uint32_t code[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(bf16_lo(w[2 * e]) / sc, bf16_hi(w[2 * e]) / sc), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(bf16_lo(w[2 * e + 1]) / sc, bf16_hi(w[2 * e + 1]) / sc), __NV_SATFINITE,
+                __NV_E4M3);
+            code[e] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+          }
+          uint2* dst = static_cast<uint2*>(h ? v_cache : k_cache) + slot * row_units + j;
+          *dst = make_uint2(code[0], code[1]);
+        }
+      } else {
+        static_cast<uint4*>(k_cache)[slot * row_units + j] = kv;
+        static_cast<uint4*>(v_cache)[slot * row_units + j] = vv;
+      }
     }
   }
 }
@@ -134,7 +159,8 @@ __global__ void __launch_bounds__(128) pa_append_rows_kernel(
 int append_rows_impl(const void* k_new, const void* v_new, const int32_t* block_tables,
                      const int32_t* context_lens, void* k_cache, void* v_cache, int num_seqs,
                      int num_queries, int num_kv_heads, int head_size, int block_size,
-                     int max_blocks_per_seq, int num_physical_blocks, void* stream, int32_t* error_flag) {
+                     int max_blocks_per_seq, int num_physical_blocks, void* stream, int32_t* error_flag,
+                     bool kv_fp8, float k_scale, float v_scale) {
   const long long n = (long long)num_seqs * num_queries;
   if (n <= 0) return PA_OK;
   cudaLaunchConfig_t cfg = {};
@@ -146,11 +172,16 @@ int append_rows_impl(const void* k_new, const void* v_new, const int32_t* block_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, pa_append_rows_kernel, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-      block_tables, context_lens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_seqs,
-      num_queries, block_size, max_blocks_per_seq, num_kv_heads * head_size * 2 / 16, num_physical_blocks,
-      error_flag);
+  const int units = num_kv_heads * head_size * 2 / 16;
+  const cudaError_t e =
+      kv_fp8 ? cudaLaunchKernelEx(&cfg, pa_append_rows_kernel<true>, static_cast<const uint4*>(k_new),
+                                  static_cast<const uint4*>(v_new), block_tables, context_lens, k_cache, v_cache,
+                                  num_seqs, num_queries, block_size, max_blocks_per_seq, units,
+                                  num_physical_blocks, k_scale, v_scale, error_flag)
+             : cudaLaunchKernelEx(&cfg, pa_append_rows_kernel<false>, static_cast<const uint4*>(k_new),
+                                  static_cast<const uint4*>(v_new), block_tables, context_lens, k_cache, v_cache,
+                                  num_seqs, num_queries, block_size, max_blocks_per_seq, units,
+                                  num_physical_blocks, 1.f, 1.f, error_flag);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_append_rows_kernel");
   return PA_OK;
 }

@@ -141,7 +141,7 @@ def test_decode_fp8_append_rejects_bad_arguments_on_host(lib, kw, code):
         (dict(v_new=24), binding.PA_ERR_INVALID_ARG),  # misaligned
         (dict(dtype=binding.PA_F32), binding.PA_ERR_UNSUPPORTED),
         (dict(num_queries=0), binding.PA_ERR_INVALID_ARG),
-        (dict(num_queries=3), binding.PA_ERR_UNSUPPORTED),  # group 8 x 3 queries > 16
+        (dict(num_queries=5), binding.PA_ERR_UNSUPPORTED),  # group 8 x 5 queries = 40 > 32 columns
     ],
 )
 def test_decode_mq_append_rejects_bad_arguments_on_host(lib, kw, code):

@@ -62,3 +62,24 @@ def test_unique_bytes_count_a_shared_prefix_once():
     sharing = (w.context_lens.numpy() >= 64)[::2].sum()  # even sequences share the 64-token prefix
     assert sharing >= 2
     assert bench.unique_kv_bytes(w, 2) == by["kv_logical"] - (sharing - 1) * 64 * 4096
+
+
+def test_step_bytes_for_fp8_pools_and_several_queries():
+    """Hand count for a tiny batch: contexts 1, 3 and 20 tokens, 2 KV heads of
+    64 dims (128 elements per row), 4 query heads, 2 queries per sequence."""
+    sp = workloads.spec("llama3_8b", num_seqs=3, num_heads=4, num_kv_heads=2, head_size=64, max_context=32,
+                        pool_blocks=0)
+    w = workloads.make_workload(sp, prewritten=False, context_lens=[1, 3, 20])
+    row = 2 * 64
+    tables = 4 * (1 + 1 + 2) + 4 * 3
+    # bf16 pools, one query: K+V 24 tokens x 2 rows x 2 B; q and out; 3 new rows read and written.
+    by = bench.step_bytes(w)
+    assert by["decode"] == 24 * 2 * row * 2 + 2 * 3 * 4 * 64 * 2 + tables
+    assert by["write"] == 3 * 2 * row * (2 + 2) + 8 * 3
+    # FP8 pools, two queries: one byte per pool element; the first sequence
+    # has only one position for its two new tokens (5 new rows in all).
+    by = bench.step_bytes(w, queries=2, kv_fp8=True)
+    assert by["kv_logical"] == 24 * 2 * row
+    assert by["decode"] == 24 * 2 * row + 2 * 3 * 2 * 4 * 64 * 2 + tables
+    assert by["write"] == 5 * 2 * row * (2 + 1) + 8 * 3 * 2
+    assert by["step"] == by["decode"] + by["write"]

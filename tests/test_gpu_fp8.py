@@ -206,3 +206,101 @@ def test_full_size_fp8_append_sampled(name, sample):
     want = ofp8.decode_fp8(w.q[sample].double().numpy(), k_ref, v_ref, bt2, ctx2, w.scale, bs, k_scale, v_scale)
     assert_close(out_b[sample], want, "bf16", f"fp8 full {name}")
     assert torch.isfinite(out_b).all()
+
+
+# ---- several query tokens per sequence over FP8 pools ----
+
+import oracle  # noqa: E402
+
+MQ_CASES = {
+    # (spec, Q): (query, head) columns per KV head 8 (one warp), 16, 12, 32, 24, 20
+    "llama_q2": (SMALL["llama3_8b"], 2),
+    "llama_q4": (SMALL["llama3_8b"], 4),
+    "long_q3": (SMALL["long_split"], 3),
+    "gqa8_q4": (SMALL["gqa8_bs32"], 4),
+    "gqa8_d64_q3": (SMALL["gqa8_d64"], 3),
+    "llama_bs24_q5": (SMALL["llama_bs24"], 5),
+}
+
+
+def _mq_queries(w, Q, seed):
+    S, H, D = w.q.shape
+    rng = np.random.default_rng([w.spec.seed, 79, Q, seed])
+    return torch.from_numpy(rng.standard_normal((S, Q, H, D), dtype=np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("name", list(MQ_CASES))
+@pytest.mark.parametrize("num_ranges", [0, 1, 5])
+def test_fp8_multi_query_matches_oracle(name, num_ranges):
+    sp, Q = MQ_CASES[name]
+    w = workloads.make_workload(sp, prewritten=True)
+    k_scale, v_scale = 0.5, 0.25
+    kcode = _codes_of_pool(w, w.k_cache, k_scale)
+    vcode = _codes_of_pool(w, w.v_cache, v_scale)
+    q = _mq_queries(w, Q, 0)
+    out = binding.decode_fp8_multi(q.cuda(), torch.from_numpy(kcode).cuda(), torch.from_numpy(vcode).cuda(),
+                                   w.block_tables.cuda(), w.context_lens.cuda(), w.scale, k_scale, v_scale,
+                                   num_ranges=num_ranges)
+    torch.cuda.synchronize()
+    want = oracle.decode_multi(q.double().numpy(), ofp8.e4m3_decode(kcode) * k_scale,
+                               ofp8.e4m3_decode(vcode) * v_scale, w.block_tables.numpy(), w.context_lens.numpy(),
+                               w.scale, sp.block_size)
+    assert_close(out, want, "bf16", f"fp8 mq {name} R={num_ranges}")
+
+
+def test_fp8_multi_query_with_one_query_equals_fp8_decode():
+    w = workloads.make_workload(SMALL["llama3_8b"], prewritten=True)
+    kcode = torch.from_numpy(_codes_of_pool(w, w.k_cache, 0.5)).cuda()
+    vcode = torch.from_numpy(_codes_of_pool(w, w.v_cache, 0.5)).cuda()
+    bt, cl = w.block_tables.cuda(), w.context_lens.cuda()
+    a = binding.decode_fp8_multi(w.q[:, None].contiguous().cuda(), kcode, vcode, bt, cl, w.scale, 0.5, 0.5)
+    b = binding.decode_fp8(w.q.cuda(), kcode, vcode, bt, cl, w.scale, 0.5, 0.5)
+    torch.cuda.synchronize()
+    assert torch.equal(a[:, 0], b)
+
+
+@pytest.mark.parametrize("name", ["llama_q2", "llama_q4", "gqa8_q4", "gqa8_d64_q3", "llama_bs24_q5"])
+@pytest.mark.parametrize("num_ranges", [0, 997])
+def test_fp8_mq_append_equals_write_then_decode(name, num_ranges):
+    """pa_decode_fp8_mq_append: the Q new rows' quantising write fused into the
+    decode (one launch up to 8 columns per KV head, a row-writing kernel
+    chained ahead above that) gives the pools and output of
+    pa_write_cache_fp8 + pa_decode_fp8_mq bit for bit."""
+    sp, Q = MQ_CASES[name]
+    w = workloads.make_workload(sp, prewritten=True)
+    k_scale, v_scale = 0.37, 2.5
+    kcode = _codes_of_pool(w, w.k_cache, k_scale)
+    vcode = _codes_of_pool(w, w.v_cache, v_scale)
+    S = sp.num_seqs
+    bs = sp.block_size
+    rng = np.random.default_rng([sp.seed, 80, Q])
+    Hk, D = w.k_cache.shape[2], w.k_cache.shape[3]
+    kn = torch.from_numpy(rng.standard_normal((S * Q, Hk, D), dtype=np.float32) * 2).to(torch.bfloat16)
+    vn = torch.from_numpy(rng.standard_normal((S * Q, Hk, D), dtype=np.float32) * 2).to(torch.bfloat16)
+    slots = np.full(S * Q, -1, dtype=np.int64)
+    for s, c in enumerate(w.context_lens.tolist()):
+        for i in range(Q):
+            pos = c - Q + i
+            if pos >= 0:
+                slots[s * Q + i] = int(w.block_tables[s, pos // bs]) * bs + pos % bs
+                kcode[slots[s * Q + i] // bs, slots[s * Q + i] % bs] = NAN_CODE  # poison until written
+                vcode[slots[s * Q + i] // bs, slots[s * Q + i] % bs] = NAN_CODE
+    q = _mq_queries(w, Q, 1).cuda()
+    bt, cl = w.block_tables.cuda(), w.context_lens.cuda()
+    ka, va = torch.from_numpy(kcode).cuda(), torch.from_numpy(vcode).cuda()
+    binding.write_cache_fp8(kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda(), ka, va, k_scale, v_scale)
+    out_a = binding.decode_fp8_multi(q, ka, va, bt, cl, w.scale, k_scale, v_scale, num_ranges=num_ranges)
+    kb, vb = torch.from_numpy(kcode).cuda(), torch.from_numpy(vcode).cuda()
+    out_b = binding.decode_fp8_multi_append(q, kn.cuda(), vn.cuda(), kb, vb, bt, cl, w.scale, k_scale, v_scale,
+                                            num_ranges=num_ranges, check_block_ids=True)
+    torch.cuda.synchronize()
+    assert torch.equal(kb, ka) and torch.equal(vb, va)
+    assert torch.equal(out_b.view(torch.int16), out_a.view(torch.int16))
+    # The written codes are the oracle quantiser's.
+    k_ref, v_ref = ofp8.write_cache_fp8(kcode, vcode, kn.float().numpy(), vn.float().numpy(), slots, bs, k_scale,
+                                        v_scale)
+    assert np.array_equal(kb.cpu().numpy(), k_ref) and np.array_equal(vb.cpu().numpy(), v_ref)
+    want = oracle.decode_multi(q.double().cpu().numpy(), ofp8.e4m3_decode(k_ref) * k_scale,
+                               ofp8.e4m3_decode(v_ref) * v_scale, w.block_tables.numpy(), w.context_lens.numpy(),
+                               w.scale, bs)
+    assert_close(out_b, want, "bf16", f"fp8 mq append {name}")

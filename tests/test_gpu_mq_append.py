@@ -92,9 +92,10 @@ def test_mq_append_block_sizes(Q, block_size):
     _check(workloads.spec("llama3_8b", **dict(SMALL_LLAMA, block_size=block_size)), Q, what=f"Q={Q} bs={block_size}")
 
 
-# More than 8 (query, head) columns per KV head: two warps of a KV head patch
-# the same new rows.
-@pytest.mark.parametrize("heads, kv_heads, Q", [(8, 1, 2), (10, 2, 3), (32, 8, 3), (64, 8, 2)])
+# More than 8 (query, head) columns per KV head (two to four warps per KV
+# head): the rows are written by their own kernel ahead of the decode.
+@pytest.mark.parametrize("heads, kv_heads, Q", [(8, 1, 2), (10, 2, 3), (32, 8, 3), (64, 8, 2), (64, 8, 3),
+                                                 (64, 8, 4), (32, 8, 5)])
 @pytest.mark.parametrize("num_ranges", [0, 1, 5])
 def test_mq_append_split_columns(heads, kv_heads, Q, num_ranges):
     sp = workloads.spec("llama3_8b", num_heads=heads, num_kv_heads=kv_heads, num_seqs=7, ctx_lo=1, ctx_hi=300,

@@ -52,7 +52,7 @@ def test_multi_query_llama_shaped(Q, num_ranges):
     assert_close(out, _oracle(w, q), "bf16", f"Q={Q} R={num_ranges}")
 
 
-@pytest.mark.parametrize("Q", [1, 2])
+@pytest.mark.parametrize("Q", [1, 2, 3, 4])
 @pytest.mark.parametrize("D", [64, 128])
 def test_multi_query_gqa8(Q, D):
     w, q = _case("gqa8_70b", Q, num_seqs=6, ctx_lo=1, ctx_hi=300, max_context=304, head_size=D)
@@ -72,9 +72,11 @@ def test_multi_query_block_sizes(Q, block_size):
     assert_close(out, _oracle(w, q), "bf16", f"Q={Q} bs={block_size}")
 
 
-# More than 8 (query, head) columns per KV head: two warps per KV head, one of
-# them with padding columns when G * Q is not 16.
-@pytest.mark.parametrize("heads, kv_heads, Q", [(8, 1, 2), (12, 2, 2), (10, 2, 3), (32, 8, 3)])
+# More than 8 (query, head) columns per KV head: two to four warps per KV head
+# (8 columns each), the last with padding columns when G * Q is not a multiple
+# of 8: 16, 12, 15, 12, 20 (three warps), 24, 32 (four warps), 28, 32 columns.
+@pytest.mark.parametrize("heads, kv_heads, Q", [(8, 1, 2), (12, 2, 2), (10, 2, 3), (32, 8, 3), (32, 8, 5),
+                                                 (64, 8, 3), (64, 8, 4), (14, 2, 4), (16, 2, 4)])
 @pytest.mark.parametrize("num_ranges", [0, 1, 5])
 def test_multi_query_split_columns(heads, kv_heads, Q, num_ranges):
     w, q = _case("llama3_8b", Q, seed=heads, num_heads=heads, num_kv_heads=kv_heads, num_seqs=7, ctx_lo=1,
@@ -128,7 +130,7 @@ def test_one_query_equals_pa_decode():
 
 
 def test_rejects_unsupported_shapes():
-    w, q = _case("llama3_8b", 5, **SMALL_LLAMA)  # G=4 x 5 queries = 20 > 16
+    w, q = _case("llama3_8b", 9, **SMALL_LLAMA)  # G=4 x 9 queries = 36 > 32 columns
     g = to_device(w)
     with pytest.raises(binding.PagedAttnError) as e:
         binding.decode_multi(q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"], g["context_lens"], w.scale)
