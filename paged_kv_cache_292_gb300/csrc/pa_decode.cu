@@ -284,7 +284,7 @@ int launch_typed(const DecodeParams& prm, const Plan& pl, int dev, cudaStream_t 
     if (dev >= 0 && dev < kTrackedDevices) configured[dev].store(true, std::memory_order_release);
   }
   cudaError_t e =
-      launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg * pl.split + 1)), pl.smem, stream, prm);
+      launch_pdl(kern, dim3(pl.R * pl.HG), dim3(32 * (pl.Hg * pl.split + kProducers)), pl.smem, stream, prm);
   if (e != cudaSuccess) return cuda_fail(e, "launch pa_decode_kernel");
   return PA_OK;
 }

@@ -63,6 +63,10 @@ namespace pa {
 constexpr int kMaxGroupHeads = 8;  // KV heads per CTA (one consumer warp each)
 constexpr int kMaxQueryGroup = 8;  // query heads per KV head (MMA N extent)
 constexpr int kMaxColumns = 32;    // (query, head) columns per KV head: four consumer warps of 8
+// Producer warps per CTA.  They share the walk over the range's tiles and
+// take alternate tiles for the per-tile work (block lookup, stage wait, arm,
+// copies), so two tiles' issue latencies overlap.
+constexpr int kProducers = 2;
 constexpr int kRowSkew = 16;       // fp32 stages: bytes between staged rows beyond the row itself
 constexpr uint32_t kLine = 128;    // tensor-core stages: bytes per swizzled line
 constexpr int kMaxRowBytes = 2048;  // bytes of one staged token row (K or V)
@@ -414,26 +418,39 @@ struct MmaConsumerMQ {
   __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
                                        int nvalid, int tok0, int ctx, int G, int Q,
                                        float scale_log2, int lane) {
-    // Scores accumulate in two independent chains (even / odd k-steps) that
-    // are added at the end: with one 8-column tile per warp, a single chain
-    // would serialise all KS MMAs.
-    float c[NT][4], c2[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) c[nt][i] = c2[nt][i] = 0.f;
+    // All K fragments are loaded first, then the scores accumulate in four
+    // independent chains (k-step mod 4) added at the end: with one 8-column
+    // tile per warp a single chain would serialise all KS MMAs.  The V
+    // fragments are loaded right after, so their latency overlaps the softmax.
+    constexpr int NCH = KS < 4 ? KS : 4;
+    uint32_t kf[KS][4], vf[KS][4];
     const RowPtr<NC> kp(k_half, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines);
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t a[4];
-      ldmatrix_x4(a, kp.at(ks));
+    for (int ks = 0; ks < KS; ++ks) ldmatrix_x4(kf[ks], kp.at(ks));
+    float cc[NCH][NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816((ks & 1) ? c2[nt] : c[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
-    }
+    for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cc[ch][nt][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(cc[ks % NCH][nt], kf[ks], qb[nt][ks][0], qb[nt][ks][1]);
+    const RowPtr<NC> vp(v_half, (lane & 7) + (lane >> 4) * 8, uh + ((lane >> 3) & 1), lines);
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) ldmatrix_x4_trans(vf[mt], vp.at(mt));
+    float c[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c[nt][i] += c2[nt][i];
+      for (int i = 0; i < 4; ++i) {
+        float v = cc[0][nt][i];
+#pragma unroll
+        for (int ch = 1; ch < NCH; ++ch) v += cc[ch][nt][i];
+        c[nt][i] = v;
+      }
     const int r0 = lane >> 2;
     const int t0 = tok0 + r0, t1 = t0 + 8;
     uint32_t pb0[NT], pb1[NT], rb0[NT], rb1[NT];
@@ -477,7 +494,6 @@ struct MmaConsumerMQ {
       rb0[nt] = movmatrix_trans(r_top);
       rb1[nt] = movmatrix_trans(r_bot);
     }
-    const RowPtr<NC> vp(v_half, (lane & 7) + (lane >> 4) * 8, uh + ((lane >> 3) & 1), lines);
     const int t2 = 2 * (lane & 3);
     uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
     if (nvalid < kTile) {
@@ -501,16 +517,136 @@ struct MmaConsumerMQ {
     }
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
-      uint32_t a[4];
-      ldmatrix_x4_trans(a, vp.at(mt));
-      a[0] &= keep_lo;
-      a[1] &= keep_lo;
-      a[2] &= keep_hi;
-      a[3] &= keep_hi;
+      vf[mt][0] &= keep_lo;
+      vf[mt][1] &= keep_lo;
+      vf[mt][2] &= keep_hi;
+      vf[mt][3] &= keep_hi;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][mt], vf[mt], pb0[nt], pb1[nt]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][mt], vf[mt], rb0[nt], rb1[nt]);
+  }
+
+  // Two consecutive tiles of one segment in one pass (the first full, from
+  // tok0; the second with nvalid1 tokens from tok0 + 16): the two tiles'
+  // score chains interleave and one softmax update covers all 32 tokens.
+  __device__ __forceinline__ void tile2(uint32_t k_half0, uint32_t v_half0, uint32_t k_half1, uint32_t v_half1,
+                                        uint32_t lines, int uh, int nvalid1, int tok0, int ctx, int G, int Q,
+                                        float scale_log2, int lane) {
+    const RowPtr<NC> kp0(k_half0, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines);
+    const RowPtr<NC> kp1(k_half1, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines);
+    float cc[2][2][NT][4];
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) cc[tt][ch][nt][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a0[4], a1[4];
+      ldmatrix_x4(a0, kp0.at(ks));
+      ldmatrix_x4(a1, kp1.at(ks));
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        mma_bf16_16816(acc[nt][mt], a, pb0[nt], pb1[nt]);
-        mma_bf16_16816(acc[nt][mt], a, rb0[nt], rb1[nt]);
+        mma_bf16_16816(cc[0][ks & 1][nt], a0, qb[nt][ks][0], qb[nt][ks][1]);
+        mma_bf16_16816(cc[1][ks & 1][nt], a1, qb[nt][ks][0], qb[nt][ks][1]);
+      }
+    }
+    const int r0 = lane >> 2;
+    uint32_t pb[2][NT][4];  // per tile: P^T hi rows 0-7, 8-15, then lo rows 0-7, 8-15
+    float alpha_a[NT], alpha_b[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
+      const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
+      const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
+      float sv[2][4];
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const int t0 = tok0 + 16 * tt + r0, t1 = t0 + 8;
+        const int nv = tt ? nvalid1 : kTile;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sv[tt][i] = (cc[tt][0][nt][i] + cc[tt][1][nt][i]) * scale_log2;
+        if (r0 >= nv || t0 > lim_a) sv[tt][0] = -INFINITY;
+        if (r0 >= nv || t0 > lim_b) sv[tt][1] = -INFINITY;
+        if (r0 + 8 >= nv || t1 > lim_a) sv[tt][2] = -INFINITY;
+        if (r0 + 8 >= nv || t1 > lim_b) sv[tt][3] = -INFINITY;
+      }
+      float mx_a = fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2]));
+      float mx_b = fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]));
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, o));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, o));
+      }
+      const float mn_a = fmaxf(m_a[nt], mx_a), mn_b = fmaxf(m_b[nt], mx_b);
+      const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
+      const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
+      alpha_a[nt] = exp2f(m_a[nt] - base_a);
+      alpha_b[nt] = exp2f(m_b[nt] - base_b);
+      m_a[nt] = mn_a;
+      m_b[nt] = mn_b;
+      float la = 0.f, lb = 0.f;
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const float p0 = exp2f(sv[tt][0] - base_a), p1 = exp2f(sv[tt][1] - base_b);
+        const float p2 = exp2f(sv[tt][2] - base_a), p3 = exp2f(sv[tt][3] - base_b);
+        const uint32_t p_top = pack_bf16x2(p0, p1), p_bot = pack_bf16x2(p2, p3);
+        const uint32_t r_top = pack_bf16x2(p0 - bf16_lo(p_top), p1 - bf16_hi(p_top));
+        const uint32_t r_bot = pack_bf16x2(p2 - bf16_lo(p_bot), p3 - bf16_hi(p_bot));
+        la += p0 + p2;
+        lb += p1 + p3;
+        pb[tt][nt][0] = movmatrix_trans(p_top);
+        pb[tt][nt][1] = movmatrix_trans(p_bot);
+        pb[tt][nt][2] = movmatrix_trans(r_top);
+        pb[tt][nt][3] = movmatrix_trans(r_bot);
+      }
+      l_a[nt] = l_a[nt] * alpha_a[nt] + la;
+      l_b[nt] = l_b[nt] * alpha_b[nt] + lb;
+    }
+    const int t2 = 2 * (lane & 3);
+    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+    if (nvalid1 < kTile) {
+      keep_lo = (t2 < nvalid1 ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid1 ? 0xffff0000u : 0u);
+      keep_hi = (t2 + 8 < nvalid1 ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid1 ? 0xffff0000u : 0u);
+    }
+    bool moved = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) moved |= (alpha_a[nt] != 1.f) || (alpha_b[nt] != 1.f);
+    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[nt][mt][0] *= alpha_a[nt];
+          acc[nt][mt][1] *= alpha_b[nt];
+          acc[nt][mt][2] *= alpha_a[nt];
+          acc[nt][mt][3] *= alpha_b[nt];
+        }
+    }
+    const RowPtr<NC> vp0(v_half0, (lane & 7) + (lane >> 4) * 8, uh + ((lane >> 3) & 1), lines);
+    const RowPtr<NC> vp1(v_half1, (lane & 7) + (lane >> 4) * 8, uh + ((lane >> 3) & 1), lines);
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t v0[4], v1[4];
+      ldmatrix_x4_trans(v0, vp0.at(mt));
+      ldmatrix_x4_trans(v1, vp1.at(mt));
+      v1[0] &= keep_lo;
+      v1[1] &= keep_lo;
+      v1[2] &= keep_hi;
+      v1[3] &= keep_hi;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_bf16_16816(acc[nt][mt], v0, pb[0][nt][0], pb[0][nt][1]);
+        mma_bf16_16816(acc[nt][mt], v1, pb[1][nt][0], pb[1][nt][1]);
+        mma_bf16_16816(acc[nt][mt], v0, pb[0][nt][2], pb[0][nt][3]);
+        mma_bf16_16816(acc[nt][mt], v1, pb[1][nt][2], pb[1][nt][3]);
       }
     }
   }
@@ -641,21 +777,28 @@ struct MmaConsumerF8 {
 #pragma unroll
     for (int j = 0; j < KS / 2; ++j) ldmatrix_x4_trans(vr[j], va ^ ((uint32_t)(j & 3) << 5));
 
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    // Scores accumulate in four independent chains (k-step mod 4).
+    constexpr int NCH = KS < 4 ? KS : 4;
+    float cc[NCH][4];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cc[ch][i] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const uint32_t top = kr[ks >> 1][2 * (ks & 1)], bot = kr[ks >> 1][2 * (ks & 1) + 1];
       uint32_t a[4];
       e4m3x4_to_f16x2x2(top, a[0], a[2]);  // token row g: codes 0,1 | codes 2,3
       e4m3x4_to_f16x2x2(bot, a[1], a[3]);  // token row g+8
-      if (ks & 1)
-        mma_f16_16816(c1, a, qb[ks][0], qb[ks][1]);
-      else
-        mma_f16_16816(c0, a, qb[ks][0], qb[ks][1]);
+      mma_f16_16816(cc[ks % NCH], a, qb[ks][0], qb[ks][1]);
     }
+#pragma unroll
+    for (int ch = 1; ch < NCH; ++ch)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cc[0][i] += cc[ch][i];
     const int g = lane >> 2, t2 = 2 * (lane & 3);
-    float s0 = (c0[0] + c1[0]) * scale_log2, s1 = (c0[1] + c1[1]) * scale_log2;
-    float s2 = (c0[2] + c1[2]) * scale_log2, s3 = (c0[3] + c1[3]) * scale_log2;
+    float s0 = cc[0][0] * scale_log2, s1 = cc[0][1] * scale_log2;
+    float s2 = cc[0][2] * scale_log2, s3 = cc[0][3] * scale_log2;
     if (g >= nvalid) s0 = s1 = -INFINITY;
     if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
     if constexpr (MQ) {
@@ -725,6 +868,126 @@ struct MmaConsumerF8 {
       e4m3x4_to_f16x2x2(__byte_perm(bot, 0u, 0x3120), a[2], a[3]);
       mma_f16_16816(acc[mt], a, pb0, pb1);
     }
+  }
+
+  // Two consecutive tiles of one segment in one pass: the first full (16
+  // tokens from tok0), the second holding nvalid1 tokens from tok0 + 16.  Their
+  // score MMAs interleave in four independent chains and one softmax update
+  // covers all 32 tokens, so the fixed-latency steps (score reductions,
+  // exponentials, rescale) run once per pair.
+  __device__ __forceinline__ void tile2(uint32_t k_half0, uint32_t v_half0, uint32_t k_half1, uint32_t v_half1,
+                                        int nvalid1, float scale_log2, int lane, int tok0 = 0, int ctx = 0,
+                                        int G = 1, int Q = 1) {
+    const uint32_t ka[2] = {k_half0 + lane_off, k_half1 + lane_off};
+    const uint32_t va[2] = {v_half0 + lane_off, v_half1 + lane_off};
+    uint32_t kr[2][KS / 2][4];
+#pragma unroll
+    for (int j = 0; j < KS / 2; ++j)
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) ldmatrix_x4(kr[tt][j], ka[tt] ^ ((uint32_t)(j & 3) << 5));
+    float cc[2][2][4];
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cc[tt][ch][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const uint32_t top = kr[tt][ks >> 1][2 * (ks & 1)], bot = kr[tt][ks >> 1][2 * (ks & 1) + 1];
+        uint32_t a[4];
+        e4m3x4_to_f16x2x2(top, a[0], a[2]);
+        e4m3x4_to_f16x2x2(bot, a[1], a[3]);
+        mma_f16_16816(cc[tt][ks & 1], a, qb[ks][0], qb[ks][1]);
+      }
+    uint32_t vr[2][KS / 2][4];
+#pragma unroll
+    for (int j = 0; j < KS / 2; ++j)
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) ldmatrix_x4_trans(vr[tt][j], va[tt] ^ ((uint32_t)(j & 3) << 5));
+    const int g = lane >> 2, t2 = 2 * (lane & 3);
+    float sc[2][4];
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[tt][i] = (cc[tt][0][i] + cc[tt][1][i]) * scale_log2;
+    if (g >= nvalid1) sc[1][0] = sc[1][1] = -INFINITY;
+    if (g + 8 >= nvalid1) sc[1][2] = sc[1][3] = -INFINITY;
+    if constexpr (MQ) {
+      const int na = col0 + t2, nb = na + 1;
+      const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
+      const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const int t0 = tok0 + 16 * tt + g, t1 = t0 + 8;
+        if (t0 > lim_a) sc[tt][0] = -INFINITY;
+        if (t0 > lim_b) sc[tt][1] = -INFINITY;
+        if (t1 > lim_a) sc[tt][2] = -INFINITY;
+        if (t1 > lim_b) sc[tt][3] = -INFINITY;
+      }
+    }
+    float mx_a = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
+    float mx_b = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, o));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, o));
+    }
+    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+    const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
+    const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
+    const float alpha_a = exp2f(m_a - base_a), alpha_b = exp2f(m_b - base_b);
+    m_a = mn_a;
+    m_b = mn_b;
+    float pw[2][4];
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+      pw[tt][0] = exp2f(sc[tt][0] - base_a);
+      pw[tt][1] = exp2f(sc[tt][1] - base_b);
+      pw[tt][2] = exp2f(sc[tt][2] - base_a);
+      pw[tt][3] = exp2f(sc[tt][3] - base_b);
+    }
+    l_a = l_a * alpha_a + ((pw[0][0] + pw[0][2]) + (pw[1][0] + pw[1][2]));
+    l_b = l_b * alpha_b + ((pw[0][1] + pw[0][3]) + (pw[1][1] + pw[1][3]));
+    uint32_t pb[2][2];
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+      pb[tt][0] = movmatrix_trans(pack_f16x2(pw[tt][0], pw[tt][1]));
+      pb[tt][1] = movmatrix_trans(pack_f16x2(pw[tt][2], pw[tt][3]));
+    }
+    if (nvalid1 < kTile) {
+      const uint32_t keep_lo = (t2 < nvalid1 ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid1 ? 0xffff0000u : 0u);
+      const uint32_t keep_hi = (t2 + 8 < nvalid1 ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid1 ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int j = 0; j < KS / 2; ++j) {
+        vr[1][j][0] &= keep_lo;
+        vr[1][j][1] &= keep_hi;
+        vr[1][j][2] &= keep_lo;
+        vr[1][j][3] &= keep_hi;
+      }
+    }
+    if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        acc[mt][0] *= alpha_a;
+        acc[mt][1] *= alpha_b;
+        acc[mt][2] *= alpha_a;
+        acc[mt][3] *= alpha_b;
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const uint32_t top = vr[tt][mt >> 1][2 * (mt & 1)];
+        const uint32_t bot = vr[tt][mt >> 1][2 * (mt & 1) + 1];
+        uint32_t a[4];
+        e4m3x4_to_f16x2x2(__byte_perm(top, 0u, 0x3120), a[0], a[1]);
+        e4m3x4_to_f16x2x2(__byte_perm(bot, 0u, 0x3120), a[2], a[3]);
+        mma_f16_16816(acc[mt], a, pb[tt][0], pb[tt][1]);
+      }
   }
 
   // Output row pairs: acc[mt][0] / [2] are dims dd / dd+1 of column a,
@@ -1143,7 +1406,7 @@ __device__ __forceinline__ void append_new_rows_fp8(const DecodeParams& p, const
 // per warp: one warp per KV head (up to 8 columns) or p.split warps (2 to 4,
 // up to 32 columns).
 template <typename T, int D, int GMAX, int QMODE, bool KV8 = false>
-__global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
+__global__ void __launch_bounds__(32 * (kMaxGroupHeads + kProducers), 1)
     pa_decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1154,7 +1417,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
   // QMODE 2 splits each KV head's (query, head) columns over p.split warps,
   // 8 columns each (up to 32 columns: four warps).
   const int kSplit = QMODE == 2 ? p.split : 1;
-  const int NCW = Hg * kSplit;  // consumer warps; warp NCW is the producer
+  const int NCW = Hg * kSplit;  // consumer warps; warps NCW .. NCW + kProducers - 1 produce
   constexpr bool kMmaPath = (sizeof(T) == 2);  // tensor-core consumers, swizzled stages
   const Layout L = make_layout(p.stages, p.q_slots, p.q_bytes, p.stage_bytes, kMmaPath);
   long long* misc = reinterpret_cast<long long*>(smem + L.misc);  // [0,32) scratch, [32..] results
@@ -1236,8 +1499,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       kMmaPath ? ((smem_addr(smem + L.stage) + 1023u) & ~1023u) : smem_addr(smem + L.stage);
   const int G = p.group, H = p.num_heads, Hk = p.num_kv_heads, bs = p.block_size;
 
-  if (warp == NCW) {
-    // ---------------- producer ----------------
+  if (warp >= NCW) {
+    // ---------------- producers ----------------
+    const int pw = warp - NCW;  // this producer takes the tiles x with (x - a) % kProducers == pw
     // Pool element: T, or one byte for an FP8 pool.
     using KV = typename std::conditional<KV8, unsigned char, T>::type;
     const KV* kc = reinterpret_cast<const KV*>(p.k_cache);
@@ -1252,7 +1516,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     int slot = 0, seg_r0 = 0, seg_r1 = 0, seg_slot0 = 0;
     int st = 0, qi = 0;
     uint32_t ph = 0, qph = 0;
-    long long armed = 0, q_armed = 0;  // stages and query slots armed so far
+    // Stages and query slots this warp armed, with the parity of the last
+    // phase it armed on each (for the drain after a timeout).
+    uint32_t my_stages = 0u, my_stage_par = 0u, my_qs = 0u, my_q_par = 0u;
     const int t = lane & 15;
     const bool is_v = lane >= 16;
     if (kMmaPath && lane == 0) {
@@ -1311,7 +1577,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
       }
       const int flags = (new_seq ? kSegBegin : 0) | ((x == b - 1 || j == ns - 1) ? kSegEnd : 0) |
                         ((slot + 1) << 2) | (seg_slot0 << 4);
-      if (new_seq) {
+      const bool mine = kProducers == 1 || static_cast<int>((x - a) % kProducers) == pw;
+      if (new_seq && mine) {
         if (!mbar_wait_warp(qempty_bar(qi), qph ^ 1u, p.wait_limit_ns)) {
           timed_out();
           break;
@@ -1331,11 +1598,19 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
                             per_q, qb);
           }
         }
-        ++q_armed;
-        if (++qi == NQ) {
-          qi = 0;
-          qph ^= 1u;
+        my_qs |= 1u << qi;
+        my_q_par = (my_q_par & ~(1u << qi)) | (qph << qi);
+      }
+      if (new_seq && ++qi == NQ) {  // every producer follows the query ring
+        qi = 0;
+        qph ^= 1u;
+      }
+      if (!mine) {  // the other producer's tile: only follow the stage ring
+        if (++st == NS) {
+          st = 0;
+          ph ^= 1u;
         }
+        continue;
       }
       // This lane's token -> physical block (a tile spans at most 16 blocks, so
       // it always lies inside the 64-entry window).
@@ -1381,6 +1656,10 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         mbar_arrive_expect_tx(full_bar(st), __popc(copies) * (kMmaPath ? p.box_bytes : p.row_bytes));
       }
       __syncwarp();
+      if (!stall) {
+        my_stages |= 1u << st;
+        my_stage_par = (my_stage_par & ~(1u << st)) | (ph << st);
+      }
       if (ok && !stall) {
         const uint32_t dst = stages + st * p.stage_bytes + lane_dst;
         if constexpr (kMmaPath) {
@@ -1390,7 +1669,6 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
           bulk_copy_g2s(dst, src, p.row_bytes, full_bar(st));
         }
       }
-      ++armed;
       if (++st == NS) {
         st = 0;
         ph ^= 1u;
@@ -1399,13 +1677,13 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
     named_barrier_sync(1, nthreads);  // every warp has left its tile loop
     if (*abort_flag != 0 && lane == 0) {
       // A wait ran out, so the loops ended early and copies this warp started
-      // may still be landing.  Wait (again bounded) for the last phase armed on
-      // every stage and query slot, so that no copy writes into this CTA's
-      // shared memory after it has retired.
+      // may still be landing.  Wait (again bounded) for the last phase it
+      // armed on each stage and query slot, so that no copy writes into this
+      // CTA's shared memory after it has retired.
       for (int i = 0; i < NS; ++i)
-        if (armed > i) (void)mbar_wait(full_bar(i), i < st ? ph : ph ^ 1u, p.wait_limit_ns);
+        if ((my_stages >> i) & 1u) (void)mbar_wait(full_bar(i), (my_stage_par >> i) & 1u, p.wait_limit_ns);
       for (int i = 0; i < NQ; ++i)
-        if (q_armed > i) (void)mbar_wait(qfull_bar(i), i < qi ? qph : qph ^ 1u, p.wait_limit_ns);
+        if ((my_qs >> i) & 1u) (void)mbar_wait(qfull_bar(i), (my_q_par >> i) & 1u, p.wait_limit_ns);
     }
   } else {
     // ---------------- consumers ----------------
@@ -1420,6 +1698,11 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, 1>>::type>::type;
     typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
     if constexpr (KV8) cons.setup(p.lines, w * D / 16, lane);
+    // FP8 and multi-query consumers take two stages at a time when both hold
+    // the same segment (tile pairing: tile2).  Their tile math, not HBM, sets
+    // the pace; one-query bf16 decode is HBM-bound and keeps its 3-stage ring
+    // free for copies.
+    constexpr bool kPair = kMma && (KV8 || QMODE > 0);
     for (long long x = a; x < b; ++x) {
       if (!mbar_wait_warp(full_bar(st), ph, p.wait_limit_ns)) {
         timed_out();
@@ -1458,7 +1741,45 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
             append_new_rows<D>(p, mt, rows, kv_head, w, k_half, v_half, lane);
         }
       }
-      if constexpr (KV8 && QMODE > 0) {
+      // A tile that does not end its segment is followed, in the next stage,
+      // by the same segment's next tile: pair them.
+      bool paired = false;
+      StageMeta me = mt;  // the pass's last tile (it carries the segment end)
+      int st_last = st;
+      if constexpr (kPair) {
+        if (!(mt.flags & kSegEnd)) {
+          const int st2 = st + 1 == NS ? 0 : st + 1;
+          const uint32_t ph2 = st + 1 == NS ? ph ^ 1u : ph;
+          if (!mbar_wait_warp(full_bar(st2), ph2, p.wait_limit_ns)) {
+            timed_out();
+            break;
+          }
+          me = meta[st2];
+          const uint32_t k_half2 = stages + st2 * p.stage_bytes;
+          const uint32_t v_half2 = k_half2 + kTile * p.lines * kLine;
+          if constexpr (QMODE < 2) {
+            if (me.newfirst >= 0) {
+              if constexpr (KV8)
+                append_new_rows_fp8<D>(p, me, stage_rows + st2 * kTile, kv_head, w, k_half2, v_half2, lane);
+              else
+                append_new_rows<D>(p, me, stage_rows + st2 * kTile, kv_head, w, k_half2, v_half2, lane);
+            }
+          }
+          if constexpr (KV8 && QMODE > 0)
+            cons.tile2(k_half, v_half, k_half2, v_half2, me.nvalid, p.scale_log2, lane, mt.tok0, mt.ctx, G,
+                       p.num_queries);
+          else if constexpr (KV8)
+            cons.tile2(k_half, v_half, k_half2, v_half2, me.nvalid, p.scale_log2, lane);
+          else
+            cons.tile2(k_half, v_half, k_half2, v_half2, p.lines, uh, me.nvalid, mt.tok0, mt.ctx, G,
+                       p.num_queries, p.scale_log2, lane);
+          paired = true;
+          st_last = st2;
+          ++x;
+        }
+      }
+      if (paired) {
+      } else if constexpr (KV8 && QMODE > 0) {
         cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane, mt.tok0, mt.ctx, G, p.num_queries);
       } else if constexpr (KV8) {
         cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane);
@@ -1472,15 +1793,22 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + 1), 1)
         cons.tile(kb, kb + kTile * p.pitch, p.pitch, mt.nvalid, p.scale_log2, G, lane);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(st));
-      if (mt.flags & kSegEnd) {
-        const int slot = ((mt.flags >> 2) & 3) - 1;
-        cons.finish(p, mt.seq, kv_head, slot, r, lane);
+      if (lane == 0) {
+        mbar_arrive(empty_bar(st));
+        if (paired) mbar_arrive(empty_bar(st_last));
+      }
+      if (me.flags & kSegEnd) {
+        const int slot = ((me.flags >> 2) & 3) - 1;
+        cons.finish(p, me.seq, kv_head, slot, r, lane);
         if (slot >= 0)
-          arrive_and_merge<T, D, (QMODE > 0)>(p, mt.seq, kv_head, mt.r0, mt.r1, (mt.flags >> 4) & 1, lane,
+          arrive_and_merge<T, D, (QMODE > 0)>(p, me.seq, kv_head, me.r0, me.r1, (me.flags >> 4) & 1, lane,
                                               kSplit);
       }
       if (++st == NS) {
+        st = 0;
+        ph ^= 1u;
+      }
+      if (paired && ++st == NS) {
         st = 0;
         ph ^= 1u;
       }
