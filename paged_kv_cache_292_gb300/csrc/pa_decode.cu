@@ -127,6 +127,12 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int 
   if (pl->stages == 0)
     return fail(PA_ERR_UNSUPPORTED, "decode stages (%u bytes each) do not fit in %d bytes of shared memory",
                 pl->stage_bytes, dev.max_smem_optin);
+  // Consumers that take two tiles per pass (FP8 pools; bf16 with a KV head's
+  // columns split over several warps) hold two stages at once: they need four
+  // or more.  Their rows are at most 1 KiB, so every shape they accept has.
+  const bool pairs = mma && (elt == 1 || pl->split >= 2);
+  if (pairs && pl->stages < 4)
+    return fail(PA_ERR_UNSUPPORTED, "decode: %d stages of %u bytes, four needed", pl->stages, pl->stage_bytes);
   workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, pl->R, pl, num_queries);
   return PA_OK;
 }

@@ -6,15 +6,17 @@
 // length (step 2), gather K/V from the scattered physical blocks (step 3),
 // attend with the step's query (step 4) and write the output (step 5).  The
 // same section's "精妙之处" asks for the gather to be planned up front and for
-// copies to overlap compute on the GPU's separate copy engine; here that is a
-// producer warp driving the TMA engine's copies into a ring of shared-memory
-// stages while consumer warps compute on earlier stages.
+// copies to overlap compute on the GPU's separate copy engine; here that is
+// two producer warps driving the TMA engine's copies into a ring of
+// shared-memory stages while consumer warps compute on earlier stages.
 //
 // Kernel 1 (pa_decode_kernel), one CTA per (token range, KV-head group):
 //   * The flattened tile list of the batch is cut into equal ranges (see
 //     pa_schedule.h), so every CTA moves the same K/V bytes.
-//   * The last warp (the producer) walks the range tile by tile.  For each tile of
-//     16 tokens it looks up the block ids and copies K and V into the stage.
+//   * The last two warps (the producers) walk the range tile by tile; both
+//     follow every tile's bookkeeping and each takes alternate tiles: for a
+//     tile of 16 tokens it looks up the block ids and copies K and V into the
+//     tile's stage.
 //     A token row is the `Hg` KV heads of the CTA's group, contiguous in the pool
 //     ([block, slot, head, dim] layout), e.g. 2 KiB for 8 heads x 128 x bf16.
 //     Tensor-core paths (bf16, FP8): one tensor-map box per run of
@@ -30,12 +32,16 @@
 //     to 8), online softmax in registers (running max and sum in the exp2
 //     domain), then O^T[D x 8] += V^T[D x 16] * P^T[16 x 8], with P^T obtained
 //     from the score fragment by movmatrix.  FP8 pools: codes widened to f16
-//     (MmaConsumerF8).  fp32: the same on CUDA cores.
+//     (MmaConsumerF8).  fp32: the same on CUDA cores.  FP8 consumers, and bf16
+//     ones that share a KV head's columns with other warps, take two tiles of
+//     one segment per pass when the ring has four or more stages (tile2).
 //   * Appending calls also write the step's new tokens of each sequence: the
 //     consumer warps put them into the staged tile and into the pool
-//     (append_new_rows).  Not with two consumer warps per KV head, where that
-//     code slowed the consumers' tile loop: the host then writes the rows with
-//     a separate kernel ahead of the decode.
+//     (append_new_rows).  Not with several consumer warps per KV head, where
+//     that code slowed the consumers' tile loop: the host then writes the rows
+//     with a separate kernel ahead of the decode.
+//   * Every wait is bounded; a wait that runs out sets PA_DEVERR_TIMEOUT, and
+//     the producers let the copies they started land before the CTA retires.
 //   * A sequence wholly inside the range is written to `out` directly.  A
 //     sequence cut by range boundaries leaves one (m, l, O) partial per range
 //     and KV head; the warp that writes the last of them (an atomic ticket per
@@ -417,6 +423,113 @@ struct MmaConsumerMQ {
 
   __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
                                        int nvalid, int tok0, int ctx, int G, int Q,
+                                       float scale_log2, int lane) {
+    // Scores accumulate in two independent chains (even / odd k-steps) that
+    // are added at the end: with one 8-column tile per warp, a single chain
+    // would serialise all KS MMAs.
+    float c[NT][4], c2[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[nt][i] = c2[nt][i] = 0.f;
+    const RowPtr<NC> kp(k_half, (lane & 7) + ((lane >> 3) & 1) * 8, uh + (lane >> 4), lines);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      ldmatrix_x4(a, kp.at(ks));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816((ks & 1) ? c2[nt] : c[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[nt][i] += c2[nt][i];
+    const int r0 = lane >> 2;
+    const int t0 = tok0 + r0, t1 = t0 + 8;
+    uint32_t pb0[NT], pb1[NT], rb0[NT], rb1[NT];
+    float alpha_a[NT], alpha_b[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
+      // Last visible position of each column's query (-1: padding column).
+      const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
+      const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
+      float s0 = c[nt][0] * scale_log2, s1 = c[nt][1] * scale_log2;
+      float s2 = c[nt][2] * scale_log2, s3 = c[nt][3] * scale_log2;
+      if (r0 >= nvalid || t0 > lim_a) s0 = -INFINITY;
+      if (r0 >= nvalid || t0 > lim_b) s1 = -INFINITY;
+      if (r0 + 8 >= nvalid || t1 > lim_a) s2 = -INFINITY;
+      if (r0 + 8 >= nvalid || t1 > lim_b) s3 = -INFINITY;
+      float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, o));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, o));
+      }
+      const float mn_a = fmaxf(m_a[nt], mx_a), mn_b = fmaxf(m_b[nt], mx_b);
+      // A column may see no token of this tile (or none yet): keep -inf out of
+      // the exponent base.
+      const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
+      const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
+      alpha_a[nt] = exp2f(m_a[nt] - base_a);
+      alpha_b[nt] = exp2f(m_b[nt] - base_b);
+      m_a[nt] = mn_a;
+      m_b[nt] = mn_b;
+      const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
+      const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+      const uint32_t p_top = pack_bf16x2(p0, p1), p_bot = pack_bf16x2(p2, p3);
+      const uint32_t r_top = pack_bf16x2(p0 - bf16_lo(p_top), p1 - bf16_hi(p_top));
+      const uint32_t r_bot = pack_bf16x2(p2 - bf16_lo(p_bot), p3 - bf16_hi(p_bot));
+      l_a[nt] = l_a[nt] * alpha_a[nt] + p0 + p2;
+      l_b[nt] = l_b[nt] * alpha_b[nt] + p1 + p3;
+      pb0[nt] = movmatrix_trans(p_top);
+      pb1[nt] = movmatrix_trans(p_bot);
+      rb0[nt] = movmatrix_trans(r_top);
+      rb1[nt] = movmatrix_trans(r_bot);
+    }
+    const RowPtr<NC> vp(v_half, (lane & 7) + (lane >> 4) * 8, uh + ((lane >> 3) & 1), lines);
+    const int t2 = 2 * (lane & 3);
+    uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+    if (nvalid < kTile) {
+      keep_lo = (t2 < nvalid ? 0x0000ffffu : 0u) | (t2 + 1 < nvalid ? 0xffff0000u : 0u);
+      keep_hi = (t2 + 8 < nvalid ? 0x0000ffffu : 0u) | (t2 + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+    // Rescale the accumulators only when some running max moved (a warp vote).
+    bool moved = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) moved |= (alpha_a[nt] != 1.f) || (alpha_b[nt] != 1.f);
+    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[nt][mt][0] *= alpha_a[nt];
+          acc[nt][mt][1] *= alpha_b[nt];
+          acc[nt][mt][2] *= alpha_a[nt];
+          acc[nt][mt][3] *= alpha_b[nt];
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, vp.at(mt));
+      a[0] &= keep_lo;
+      a[1] &= keep_lo;
+      a[2] &= keep_hi;
+      a[3] &= keep_hi;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_bf16_16816(acc[nt][mt], a, pb0[nt], pb1[nt]);
+        mma_bf16_16816(acc[nt][mt], a, rb0[nt], rb1[nt]);
+      }
+    }
+  }
+
+  // The same with all K fragments loaded first, the scores in four chains
+  // and the V fragments loaded before the softmax (used when a KV head's
+  // columns are split over several warps, where it measured faster).
+  __device__ __forceinline__ void tile_hoisted(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
+                                               int nvalid, int tok0, int ctx, int G, int Q,
                                        float scale_log2, int lane) {
     // All K fragments are loaded first, then the scores accumulate in four
     // independent chains (k-step mod 4) added at the end: with one 8-column
@@ -1698,11 +1811,13 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + kProducers), 1)
         typename std::conditional<QMODE == 0, MmaConsumer<D>, MmaConsumerMQ<D, 1>>::type>::type;
     typename std::conditional<kMma, Mma, SimtConsumer<D, GMAX>>::type cons;
     if constexpr (KV8) cons.setup(p.lines, w * D / 16, lane);
-    // FP8 and multi-query consumers take two stages at a time when both hold
-    // the same segment (tile pairing: tile2).  Their tile math, not HBM, sets
-    // the pace; one-query bf16 decode is HBM-bound and keeps its 3-stage ring
-    // free for copies.
-    constexpr bool kPair = kMma && (KV8 || QMODE > 0);
+    // FP8 consumers, and bf16 ones that split a KV head's columns over
+    // several warps, take two stages at a time when both hold the same
+    // segment (tile pairing: tile2), if the ring has four or more stages.
+    // Their tile math, not HBM, sets the pace.  One-query bf16 decode and
+    // bf16 multi-query with one warp per KV head (2 KiB rows, a 3-stage ring
+    // for the common shapes) are HBM-bound and keep the ring for copies.
+    constexpr bool kPair = kMma && (KV8 || QMODE == 2);
     for (long long x = a; x < b; ++x) {
       if (!mbar_wait_warp(full_bar(st), ph, p.wait_limit_ns)) {
         timed_out();
@@ -1747,6 +1862,8 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + kProducers), 1)
       StageMeta me = mt;  // the pass's last tile (it carries the segment end)
       int st_last = st;
       if constexpr (kPair) {
+        // The ring has four or more stages here (the host plan checks it): a
+        // pair holds two, and the copies need the rest.
         if (!(mt.flags & kSegEnd)) {
           const int st2 = st + 1 == NS ? 0 : st + 1;
           const uint32_t ph2 = st + 1 == NS ? ph ^ 1u : ph;
@@ -1783,6 +1900,9 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + kProducers), 1)
         cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane, mt.tok0, mt.ctx, G, p.num_queries);
       } else if constexpr (KV8) {
         cons.tile(k_half, v_half, mt.nvalid, p.scale_log2, lane);
+      } else if constexpr (kMma && QMODE == 2) {
+        cons.tile_hoisted(k_half, v_half, p.lines, uh, mt.nvalid, mt.tok0, mt.ctx, G, p.num_queries,
+                          p.scale_log2, lane);
       } else if constexpr (kMma && QMODE > 0) {
         cons.tile(k_half, v_half, p.lines, uh, mt.nvalid, mt.tok0, mt.ctx, G, p.num_queries,
                   p.scale_log2, lane);
