@@ -181,3 +181,39 @@ def test_stall_hook_checks_its_argument(lib):
     assert lib.pa_test_stall_copy(-2, 0) == binding.PA_ERR_INVALID_ARG
     assert lib.pa_test_stall_copy(5, 1000) == binding.PA_OK
     assert lib.pa_test_stall_copy(-1, 0) == binding.PA_OK  # cleared
+
+
+@pytest.mark.parametrize(
+    "kw, code",
+    [
+        (dict(k_new=None), binding.PA_ERR_INVALID_ARG),
+        (dict(v_new=24), binding.PA_ERR_INVALID_ARG),  # misaligned
+        (dict(num_queries=0), binding.PA_ERR_INVALID_ARG),
+        (dict(num_queries=5), binding.PA_ERR_UNSUPPORTED),  # group 8 x 5 queries = 40 > 32 columns
+        (dict(k_scale=0.0), binding.PA_ERR_INVALID_ARG),
+        (dict(v_scale=float("nan")), binding.PA_ERR_INVALID_ARG),
+    ],
+)
+def test_decode_fp8_mq_append_rejects_bad_arguments_on_host(lib, kw, code):
+    a = dict(k_new=16, v_new=16, num_queries=2, k_scale=1.0, v_scale=1.0)
+    a.update(kw)
+    rc = lib.pa_decode_fp8_mq_append(16, 16, a["k_new"], a["v_new"], 16, 16, 16, 16, 1, a["num_queries"], 32, 4,
+                                     128, 16, 4, 0.1, a["k_scale"], a["v_scale"], 0, 0, None, 0, 0, None)
+    assert rc == code
+    assert lib.pa_last_error().decode()
+
+
+@pytest.mark.parametrize(
+    "kw, code",
+    [
+        (dict(query=None), binding.PA_ERR_INVALID_ARG),
+        (dict(num_queries=9, heads=16, kv_heads=4), binding.PA_ERR_UNSUPPORTED),  # 4 x 9 = 36 > 32
+        (dict(head_size=96), binding.PA_ERR_UNSUPPORTED),
+    ],
+)
+def test_decode_fp8_mq_rejects_bad_arguments_on_host(lib, kw, code):
+    a = dict(query=16, num_queries=2, heads=32, kv_heads=8, head_size=128)
+    a.update(kw)
+    rc = lib.pa_decode_fp8_mq(16, a["query"], 16, 16, 16, 16, 1, a["num_queries"], a["heads"], a["kv_heads"],
+                              a["head_size"], 16, 4, 0.1, 1.0, 1.0, 0, 0, None, 0, 0, None)
+    assert rc == code
