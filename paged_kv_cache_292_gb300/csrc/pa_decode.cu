@@ -435,7 +435,7 @@ int decode_impl_q(void* out, const void* query, const void* k_cache, const void*
   }
   take_wait_test(&prm.stall_tile, &prm.wait_limit_ns);
   if (k_new != nullptr && pl.split >= 2) {
-    // Two consumer warps per KV head: the rows are written by their own
+    // Several consumer warps per KV head: the rows are written by their own
     // kernel, chained ahead of the decode, which then only reads them.
     rc = append_rows_impl(k_new, v_new, block_tables, context_lens, const_cast<void*>(k_cache),
                           const_cast<void*>(v_cache), num_seqs, num_queries, num_kv_heads, head_size,

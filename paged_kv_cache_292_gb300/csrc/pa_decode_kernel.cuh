@@ -1324,8 +1324,8 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 // (seq, kv_head).  Takes a ticket; the warp holding the last of the r1-r0+1
 // tickets merges every partial of that sequence and KV head by log-sum-exp,
 // writes the output rows, and resets the ticket counter.  Nobody waits.
-// `arrivals`: warps writing partials per range and KV head (two when the
-// (query, head) columns of a KV head are split across two warps).
+// `arrivals`: warps writing partials per range and KV head (two to four when
+// the (query, head) columns of a KV head are split across several warps).
 template <typename T, int D, bool kMQ>
 __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, int r0, int r1,
                                  int slot0, int lane, int arrivals = 1) {
@@ -1584,7 +1584,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + kProducers), 1)
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta);
   int* stage_rows = reinterpret_cast<int*>(smem + L.rows);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 34);
-  // A pipeline wait ran out: report it and tell the producer to drain.
+  // A pipeline wait ran out: report it and tell the producers to drain.
   auto timed_out = [&]() {
     if (lane == 0) {
       report(p.error_flag, PA_DEVERR_TIMEOUT);
@@ -1933,7 +1933,7 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + kProducers), 1)
         ph ^= 1u;
       }
     }
-    named_barrier_sync(1, nthreads);  // lets the producer drain its copies after a timeout
+    named_barrier_sync(1, nthreads);  // lets the producers drain their copies after a timeout
   }
   (void)Hk;
 }
