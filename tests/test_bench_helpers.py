@@ -83,3 +83,23 @@ def test_step_bytes_for_fp8_pools_and_several_queries():
     assert by["decode"] == 24 * 2 * row + 2 * 3 * 2 * 4 * 64 * 2 + tables
     assert by["write"] == 5 * 2 * row * (2 + 1) + 8 * 3 * 2
     assert by["step"] == by["decode"] + by["write"]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """bench.py --impl reference times the oracle on the host and prints one
+    JSON line with the contract's keys (no GPU needed)."""
+    import subprocess
+    import sys
+
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny_fp32", "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=300,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "tiny_fp32"
