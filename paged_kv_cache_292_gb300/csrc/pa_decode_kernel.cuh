@@ -450,16 +450,22 @@ struct MmaConsumerMQ {
     float alpha_a[NT], alpha_b[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
-      // Last visible position of each column's query (-1: padding column).
-      const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
-      const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
       float s0 = c[nt][0] * scale_log2, s1 = c[nt][1] * scale_log2;
       float s2 = c[nt][2] * scale_log2, s3 = c[nt][3] * scale_log2;
-      if (r0 >= nvalid || t0 > lim_a) s0 = -INFINITY;
-      if (r0 >= nvalid || t0 > lim_b) s1 = -INFINITY;
-      if (r0 + 8 >= nvalid || t1 > lim_a) s2 = -INFINITY;
-      if (r0 + 8 >= nvalid || t1 > lim_b) s3 = -INFINITY;
+      if (r0 >= nvalid) s0 = s1 = -INFINITY;
+      if (r0 + 8 >= nvalid) s2 = s3 = -INFINITY;
+      // Causal limits matter only on tiles that reach the queries' own
+      // positions (ctx - Q ..); the test is the same for the whole warp.
+      if (tok0 + kTile > ctx - Q) {
+        const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
+        // Last visible position of each column's query (-1: padding column).
+        const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
+        const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
+        if (t0 > lim_a) s0 = -INFINITY;
+        if (t0 > lim_b) s1 = -INFINITY;
+        if (t1 > lim_a) s2 = -INFINITY;
+        if (t1 > lim_b) s3 = -INFINITY;
+      }
       float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -570,16 +576,22 @@ struct MmaConsumerMQ {
     float alpha_a[NT], alpha_b[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
-      // Last visible position of each column's query (-1: padding column).
-      const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
-      const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
       float s0 = c[nt][0] * scale_log2, s1 = c[nt][1] * scale_log2;
       float s2 = c[nt][2] * scale_log2, s3 = c[nt][3] * scale_log2;
-      if (r0 >= nvalid || t0 > lim_a) s0 = -INFINITY;
-      if (r0 >= nvalid || t0 > lim_b) s1 = -INFINITY;
-      if (r0 + 8 >= nvalid || t1 > lim_a) s2 = -INFINITY;
-      if (r0 + 8 >= nvalid || t1 > lim_b) s3 = -INFINITY;
+      if (r0 >= nvalid) s0 = s1 = -INFINITY;
+      if (r0 + 8 >= nvalid) s2 = s3 = -INFINITY;
+      // Causal limits matter only on tiles that reach the queries' own
+      // positions (ctx - Q ..); the test is the same for the whole warp.
+      if (tok0 + kTile > ctx - Q) {
+        const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
+        // Last visible position of each column's query (-1: padding column).
+        const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
+        const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
+        if (t0 > lim_a) s0 = -INFINITY;
+        if (t0 > lim_b) s1 = -INFINITY;
+        if (t1 > lim_a) s2 = -INFINITY;
+        if (t1 > lim_b) s3 = -INFINITY;
+      }
       float mx_a = fmaxf(s0, s2), mx_b = fmaxf(s1, s3);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -676,20 +688,27 @@ struct MmaConsumerMQ {
     float alpha_a[NT], alpha_b[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
-      const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
-      const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
       float sv[2][4];
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
-        const int t0 = tok0 + 16 * tt + r0, t1 = t0 + 8;
         const int nv = tt ? nvalid1 : kTile;
 #pragma unroll
         for (int i = 0; i < 4; ++i) sv[tt][i] = (cc[tt][0][nt][i] + cc[tt][1][nt][i]) * scale_log2;
-        if (r0 >= nv || t0 > lim_a) sv[tt][0] = -INFINITY;
-        if (r0 >= nv || t0 > lim_b) sv[tt][1] = -INFINITY;
-        if (r0 + 8 >= nv || t1 > lim_a) sv[tt][2] = -INFINITY;
-        if (r0 + 8 >= nv || t1 > lim_b) sv[tt][3] = -INFINITY;
+        if (r0 >= nv) sv[tt][0] = sv[tt][1] = -INFINITY;
+        if (r0 + 8 >= nv) sv[tt][2] = sv[tt][3] = -INFINITY;
+      }
+      if (tok0 + 2 * kTile > ctx - Q) {  // the pair reaches the queries' own positions
+        const int na = col0 + nt * 8 + 2 * (lane & 3), nb = na + 1;
+        const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
+        const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          const int t0 = tok0 + 16 * tt + r0, t1 = t0 + 8;
+          if (t0 > lim_a) sv[tt][0] = -INFINITY;
+          if (t0 > lim_b) sv[tt][1] = -INFINITY;
+          if (t1 > lim_a) sv[tt][2] = -INFINITY;
+          if (t1 > lim_b) sv[tt][3] = -INFINITY;
+        }
       }
       float mx_a = fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2]));
       float mx_b = fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]));
@@ -914,7 +933,7 @@ struct MmaConsumerF8 {
     float s2 = cc[0][2] * scale_log2, s3 = cc[0][3] * scale_log2;
     if (g >= nvalid) s0 = s1 = -INFINITY;
     if (g + 8 >= nvalid) s2 = s3 = -INFINITY;
-    if constexpr (MQ) {
+    if (MQ && tok0 + kTile > ctx - Q) {  // only tiles reaching the queries' own positions
       // Last visible position of each column's query (-1: padding column).
       const int na = col0 + t2, nb = na + 1;
       const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
@@ -1028,7 +1047,7 @@ struct MmaConsumerF8 {
       for (int i = 0; i < 4; ++i) sc[tt][i] = (cc[tt][0][i] + cc[tt][1][i]) * scale_log2;
     if (g >= nvalid1) sc[1][0] = sc[1][1] = -INFINITY;
     if (g + 8 >= nvalid1) sc[1][2] = sc[1][3] = -INFINITY;
-    if constexpr (MQ) {
+    if (MQ && tok0 + 2 * kTile > ctx - Q) {  // the pair reaches the queries' own positions
       const int na = col0 + t2, nb = na + 1;
       const int lim_a = na < G * Q ? ctx - Q + na / G : -1;
       const int lim_b = nb < G * Q ? ctx - Q + nb / G : -1;
@@ -1145,34 +1164,34 @@ struct MmaConsumerF8 {
           if (hb < G) *reinterpret_cast<float2*>(pm + (size_t)qb_ * 2) = make_float2(m_b, lb);
         }
       }
-      return;
-    }
+    } else {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int n = col0 + 2 * (lane & 3) + half;
-      if (n >= G * Q) continue;
-      int qi = 0, gh = n;
-      if constexpr (MQ) {
-        qi = n / G;
-        gh = n % G;
-      }
-      const int row = qi * H + kv_head * G + gh;
-      const float l = half ? lb : la, m = half ? m_b : m_a;
-      if (slot < 0) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)seq * Q * H + row) * D;
-        // A query with no keys (several queries, short context) gives zeros.
-        const float inv = (!MQ || l > 0.f) ? p.v_scale / l : 0.f;
+      for (int half = 0; half < 2; ++half) {
+        const int n = col0 + 2 * (lane & 3) + half;
+        if (n >= G * Q) continue;
+        int qi = 0, gh = n;
+        if constexpr (MQ) {
+          qi = n / G;
+          gh = n % G;
+        }
+        const int row = qi * H + kv_head * G + gh;
+        const float l = half ? lb : la, m = half ? m_b : m_a;
+        if (slot < 0) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)seq * Q * H + row) * D;
+          // A query with no keys (several queries, short context) gives zeros.
+          const float inv = (!MQ || l > 0.f) ? p.v_scale / l : 0.f;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt)
-          *reinterpret_cast<uint32_t*>(out + mt * 16 + 2 * g) =
-              pack_bf16x2(acc[mt][half] * inv, acc[mt][2 + half] * inv);
-      } else {
-        const size_t base = ((size_t)r * 2 + slot) * Q * H + row;
-        float* po = p.part_o + base * D;
+          for (int mt = 0; mt < KS; ++mt)
+            *reinterpret_cast<uint32_t*>(out + mt * 16 + 2 * g) =
+                pack_bf16x2(acc[mt][half] * inv, acc[mt][2 + half] * inv);
+        } else {
+          const size_t base = ((size_t)r * 2 + slot) * Q * H + row;
+          float* po = p.part_o + base * D;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt)
-          *reinterpret_cast<float2*>(po + mt * 16 + 2 * g) = make_float2(acc[mt][half], acc[mt][2 + half]);
-        if (g == 0) *reinterpret_cast<float2*>(p.part_ml + base * 2) = make_float2(m, l);
+          for (int mt = 0; mt < KS; ++mt)
+            *reinterpret_cast<float2*>(po + mt * 16 + 2 * g) = make_float2(acc[mt][half], acc[mt][2 + half]);
+          if (g == 0) *reinterpret_cast<float2*>(p.part_ml + base * 2) = make_float2(m, l);
+        }
       }
     }
   }
