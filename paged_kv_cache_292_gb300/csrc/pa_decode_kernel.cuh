@@ -282,11 +282,11 @@ struct MmaConsumer {
     // are not; guard the exponent base anyway so -inf - -inf never appears.
     const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
     const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
-    const float alpha_a = exp2f(m_a - base_a), alpha_b = exp2f(m_b - base_b);
+    const float alpha_a = ex2_ftz(m_a - base_a), alpha_b = ex2_ftz(m_b - base_b);
     m_a = mn_a;
     m_b = mn_b;
-    const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
-    const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+    const float p0 = ex2_ftz(s0 - base_a), p1 = ex2_ftz(s1 - base_b);
+    const float p2 = ex2_ftz(s2 - base_a), p3 = ex2_ftz(s3 - base_b);
     // P enters the bf16 MMA as a high and a low bf16 part (P = hi + lo to
     // about 2^-16), so the weights keep fp32-like precision.
     const uint32_t p_top = pack_bf16x2(p0, p1), p_bot = pack_bf16x2(p2, p3);
@@ -477,12 +477,12 @@ struct MmaConsumerMQ {
       // the exponent base.
       const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
       const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
-      alpha_a[nt] = exp2f(m_a[nt] - base_a);
-      alpha_b[nt] = exp2f(m_b[nt] - base_b);
+      alpha_a[nt] = ex2_ftz(m_a[nt] - base_a);
+      alpha_b[nt] = ex2_ftz(m_b[nt] - base_b);
       m_a[nt] = mn_a;
       m_b[nt] = mn_b;
-      const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
-      const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+      const float p0 = ex2_ftz(s0 - base_a), p1 = ex2_ftz(s1 - base_b);
+      const float p2 = ex2_ftz(s2 - base_a), p3 = ex2_ftz(s3 - base_b);
       const uint32_t p_top = pack_bf16x2(p0, p1), p_bot = pack_bf16x2(p2, p3);
       const uint32_t r_top = pack_bf16x2(p0 - bf16_lo(p_top), p1 - bf16_hi(p_top));
       const uint32_t r_bot = pack_bf16x2(p2 - bf16_lo(p_bot), p3 - bf16_hi(p_bot));
@@ -603,12 +603,12 @@ struct MmaConsumerMQ {
       // the exponent base.
       const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
       const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
-      alpha_a[nt] = exp2f(m_a[nt] - base_a);
-      alpha_b[nt] = exp2f(m_b[nt] - base_b);
+      alpha_a[nt] = ex2_ftz(m_a[nt] - base_a);
+      alpha_b[nt] = ex2_ftz(m_b[nt] - base_b);
       m_a[nt] = mn_a;
       m_b[nt] = mn_b;
-      const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
-      const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+      const float p0 = ex2_ftz(s0 - base_a), p1 = ex2_ftz(s1 - base_b);
+      const float p2 = ex2_ftz(s2 - base_a), p3 = ex2_ftz(s3 - base_b);
       const uint32_t p_top = pack_bf16x2(p0, p1), p_bot = pack_bf16x2(p2, p3);
       const uint32_t r_top = pack_bf16x2(p0 - bf16_lo(p_top), p1 - bf16_hi(p_top));
       const uint32_t r_bot = pack_bf16x2(p2 - bf16_lo(p_bot), p3 - bf16_hi(p_bot));
@@ -720,15 +720,15 @@ struct MmaConsumerMQ {
       const float mn_a = fmaxf(m_a[nt], mx_a), mn_b = fmaxf(m_b[nt], mx_b);
       const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
       const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
-      alpha_a[nt] = exp2f(m_a[nt] - base_a);
-      alpha_b[nt] = exp2f(m_b[nt] - base_b);
+      alpha_a[nt] = ex2_ftz(m_a[nt] - base_a);
+      alpha_b[nt] = ex2_ftz(m_b[nt] - base_b);
       m_a[nt] = mn_a;
       m_b[nt] = mn_b;
       float la = 0.f, lb = 0.f;
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
-        const float p0 = exp2f(sv[tt][0] - base_a), p1 = exp2f(sv[tt][1] - base_b);
-        const float p2 = exp2f(sv[tt][2] - base_a), p3 = exp2f(sv[tt][3] - base_b);
+        const float p0 = ex2_ftz(sv[tt][0] - base_a), p1 = ex2_ftz(sv[tt][1] - base_b);
+        const float p2 = ex2_ftz(sv[tt][2] - base_a), p3 = ex2_ftz(sv[tt][3] - base_b);
         const uint32_t p_top = pack_bf16x2(p0, p1), p_bot = pack_bf16x2(p2, p3);
         const uint32_t r_top = pack_bf16x2(p0 - bf16_lo(p_top), p1 - bf16_hi(p_top));
         const uint32_t r_bot = pack_bf16x2(p2 - bf16_lo(p_bot), p3 - bf16_hi(p_bot));
@@ -953,11 +953,11 @@ struct MmaConsumerF8 {
     const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
     const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
     const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
-    const float alpha_a = exp2f(m_a - base_a), alpha_b = exp2f(m_b - base_b);
+    const float alpha_a = ex2_ftz(m_a - base_a), alpha_b = ex2_ftz(m_b - base_b);
     m_a = mn_a;
     m_b = mn_b;
-    const float p0 = exp2f(s0 - base_a), p1 = exp2f(s1 - base_b);
-    const float p2 = exp2f(s2 - base_a), p3 = exp2f(s3 - base_b);
+    const float p0 = ex2_ftz(s0 - base_a), p1 = ex2_ftz(s1 - base_b);
+    const float p2 = ex2_ftz(s2 - base_a), p3 = ex2_ftz(s3 - base_b);
     // Weights enter the f16 MMA rounded to f16 (relative error <= 2^-11,
     // half an ulp of the 10-bit fraction), well inside the bf16 output's own
     // rounding; the running sum keeps them in fp32.
@@ -1070,16 +1070,16 @@ struct MmaConsumerF8 {
     const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
     const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a;
     const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b;
-    const float alpha_a = exp2f(m_a - base_a), alpha_b = exp2f(m_b - base_b);
+    const float alpha_a = ex2_ftz(m_a - base_a), alpha_b = ex2_ftz(m_b - base_b);
     m_a = mn_a;
     m_b = mn_b;
     float pw[2][4];
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt) {
-      pw[tt][0] = exp2f(sc[tt][0] - base_a);
-      pw[tt][1] = exp2f(sc[tt][1] - base_b);
-      pw[tt][2] = exp2f(sc[tt][2] - base_a);
-      pw[tt][3] = exp2f(sc[tt][3] - base_b);
+      pw[tt][0] = ex2_ftz(sc[tt][0] - base_a);
+      pw[tt][1] = ex2_ftz(sc[tt][1] - base_b);
+      pw[tt][2] = ex2_ftz(sc[tt][2] - base_a);
+      pw[tt][3] = ex2_ftz(sc[tt][3] - base_b);
     }
     l_a = l_a * alpha_a + ((pw[0][0] + pw[0][2]) + (pw[1][0] + pw[1][2]));
     l_b = l_b * alpha_b + ((pw[0][1] + pw[0][3]) + (pw[1][1] + pw[1][3]));
@@ -1273,9 +1273,9 @@ struct SimtConsumer {
       for (int o = 2; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float mn = fmaxf(m[h], mx);
       const float base = (mn == -INFINITY) ? 0.f : mn;
-      const float alpha = exp2f(m[h] - base);
+      const float alpha = ex2_ftz(m[h] - base);
       m[h] = mn;
-      const float pw = exp2f(sc - base);
+      const float pw = ex2_ftz(sc - base);
       l[h] = l[h] * alpha + pw;
 #pragma unroll
       for (int i = 0; i < DC; ++i) acc[h][i] *= alpha;
@@ -1424,7 +1424,7 @@ __device__ void arrive_and_merge(const DecodeParams& p, int seq, int kv_head, in
           // Several queries: a query may have no keys in some (or all)
           // partials, m = -inf; keep -inf out of the exponent base.
           const float mb = (kMQ && mnew == -INFINITY) ? 0.f : mnew;
-          const float a_old = exp2f(run_m[g] - mb), a_new = exp2f(cm[g] - mb);
+          const float a_old = ex2_ftz(run_m[g] - mb), a_new = ex2_ftz(cm[g] - mb);
           run_m[g] = mnew;
           run_l[g] = run_l[g] * a_old + cl[g] * a_new;
 #pragma unroll

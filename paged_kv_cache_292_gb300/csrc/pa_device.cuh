@@ -1,7 +1,7 @@
 // Device-side building blocks for sm_103a: mbarriers, the TMA engine's bulk
 // (untiled) and tensor-map (tiled) async copies, ldmatrix / movmatrix, the
-// bf16 and f16 tensor-core MMAs and the E4M3 widening.  Inline PTX and CUDA
-// intrinsics only; no library code.
+// bf16 and f16 tensor-core MMAs, the E4M3 widening and the SFU's 2^x.
+// Inline PTX and CUDA intrinsics only; no library code.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -10,6 +10,17 @@
 #include <stdint.h>
 
 namespace pa {
+
+// 2^x on the special-function unit with subnormal results flushed to zero
+// (PTX ex2.approx.ftz.f32).  Used for the online softmax's weights and
+// rescale factors, which are 2^(s - m) with m the running maximum: a weight
+// below 2^-126 is nothing against the maximum's own weight of 1.  Exact for
+// x = 0 (a factor of 1 leaves the accumulators unscaled) and 0 for -inf.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
