@@ -366,16 +366,9 @@ def measure(args, lib, dev, world, rank, local, cpu_baseline=True):
     if Q > 1:
         # Several new tokens per sequence (positions c-Q .. c-1): their query
         # rows, their K/V rows and their slots; the pool already holds them.
-        gen = torch.Generator().manual_seed(sp.seed + 77)
-        g["q"] = torch.randn(S, Q, H, D, generator=gen).to(w.q.dtype).to(dev)
-        g["k_new"] = torch.randn(S * Q, Hk, D, generator=gen).to(w.q.dtype).to(dev)
-        g["v_new"] = torch.randn(S * Q, Hk, D, generator=gen).to(w.q.dtype).to(dev)
-        slots = []
-        for s_, c in enumerate(w.context_lens.tolist()):
-            for i in range(Q):
-                pos = c - Q + i
-                slots.append(-1 if pos < 0 else int(w.block_tables[s_, pos // bs]) * bs + pos % bs)
-        g["slot_mapping"] = torch.tensor(slots, dtype=torch.int64, device=dev)
+        mq = workloads.multi_query_step(w, Q)
+        for k, v in zip(("q", "k_new", "v_new", "slot_mapping"), mq):
+            g[k] = v.to(dev)
     if fp8:
         # E4M3 pools (one scale per pool); the prompt's K/V quantised once here.
         k_scale = v_scale = 1.0

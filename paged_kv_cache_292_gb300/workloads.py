@@ -39,7 +39,8 @@ from typing import Optional
 import numpy as np
 import torch
 
-__all__ = ["WorkloadSpec", "Workload", "SPECS", "spec", "make_workload", "kv_bytes_per_token"]
+__all__ = ["WorkloadSpec", "Workload", "SPECS", "spec", "make_workload", "kv_bytes_per_token",
+           "multi_query_step"]
 
 # Stream tags for the seeded generators.
 _CTX, _PERM, _Q, _PREFIX_K, _PREFIX_V, _SEQ_K, _SEQ_V = 1, 2, 3, 4, 5, 10, 11
@@ -278,3 +279,27 @@ def _place(pool: torch.Tensor, block_ids, rows: torch.Tensor, bs: int) -> None:
     rem = n - full * bs
     if rem:
         pool[int(ids[full]), :rem] = rows[full * bs :]
+
+
+def multi_query_step(w: Workload, num_queries: int):
+    """Inputs of a step with ``num_queries`` new tokens per sequence, at
+    positions ctx - Q .. ctx - 1 of each sequence: their query rows
+    ``q[S, Q, H, D]``, their K/V rows ``k_new, v_new[S * Q, Hk, D]`` (row
+    s * Q + i for position ctx - Q + i) and the pool slot of each row
+    (``slots[S * Q]``, int64; -1 for a position before the sequence's start).
+    Drawn N(0, 1) from one seeded torch generator, q first, then K, then V,
+    and cast to the workload's dtype.
+    """
+    s = w.spec
+    S, H, D = w.q.shape
+    Q, Hk, bs = num_queries, s.num_kv_heads, s.block_size
+    gen = torch.Generator().manual_seed(s.seed + 77)
+    q = torch.randn(S, Q, H, D, generator=gen).to(w.q.dtype)
+    k_new = torch.randn(S * Q, Hk, D, generator=gen).to(w.q.dtype)
+    v_new = torch.randn(S * Q, Hk, D, generator=gen).to(w.q.dtype)
+    slots = []
+    for i, c in enumerate(w.context_lens.tolist()):
+        for j in range(Q):
+            pos = c - Q + j
+            slots.append(-1 if pos < 0 else int(w.block_tables[i, pos // bs]) * bs + pos % bs)
+    return q, k_new, v_new, torch.tensor(slots, dtype=torch.int64)
