@@ -87,3 +87,30 @@ def test_unwritten_slot_is_left_for_the_cache_write():
         slot = int(w.slot_mapping[s])
         assert torch.isnan(w.k_cache[slot // bs, slot % bs]).all()
         assert torch.isfinite(w.k_new[s]).all()
+
+
+@pytest.mark.parametrize("Q", [1, 2, 5])
+def test_multi_query_step_layout(Q):
+    """Q new tokens per sequence at positions ctx - Q .. ctx - 1: rows s * Q + i,
+    each row's slot is that position's place in the sequence's blocks, -1
+    before the sequence's start; the same draws every time."""
+    ctx = np.array([1, 3, 16, 17, 40, 0])
+    sp = workloads.spec("llama3_8b", num_seqs=len(ctx), max_context=48, pool_blocks=0)
+    w = workloads.make_workload(sp, prewritten=False, context_lens=ctx)
+    q, kn, vn, slots = workloads.multi_query_step(w, Q)
+    S, H, D = w.q.shape
+    assert q.shape == (S, Q, H, D) and q.dtype == w.q.dtype
+    assert kn.shape == vn.shape == (S * Q, sp.num_kv_heads, D) and kn.dtype == w.k_cache.dtype
+    assert slots.shape == (S * Q,) and slots.dtype == torch.int64
+    bs = sp.block_size
+    bt = w.block_tables.numpy()
+    for s, c in enumerate(ctx):
+        for i in range(Q):
+            pos = int(c) - Q + i
+            want = -1 if pos < 0 else int(bt[s, pos // bs]) * bs + pos % bs
+            assert int(slots[s * Q + i]) == want
+    again = workloads.multi_query_step(w, Q)
+    assert all(torch.equal(a, b) for a, b in zip((q, kn, vn, slots), again))
+    if Q == 1:
+        # One query: the newest token's slot is the workload's own slot.
+        assert torch.equal(slots[ctx > 0], w.slot_mapping[ctx > 0])
