@@ -419,6 +419,22 @@ struct MmaConsumerMQ {
     }
   }
 
+  // After a segment's finish (and merge) every state register is rewritten
+  // by the next begin_segment before it is read; writing them here tells the
+  // compiler so, which frees them for the merge.
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[nt][ks][0] = qb[nt][ks][1] = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][ks][i] = 0.f;
+      }
+      m_a[nt] = m_b[nt] = l_a[nt] = l_b[nt] = 0.f;
+    }
+  }
+
   static constexpr int NC = D * 2 > 128 ? D * 2 / 128 : 1;
 
   __device__ __forceinline__ void tile(uint32_t k_half, uint32_t v_half, uint32_t lines, int uh,
@@ -893,6 +909,19 @@ struct MmaConsumerF8 {
     }
     m_a = m_b = -INFINITY;
     l_a = l_b = 0.f;
+  }
+
+  // After a segment's finish (and merge) every state register is rewritten
+  // by the next begin_segment before it is read; writing them here tells the
+  // compiler so, which frees them for the merge.
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[ks][0] = qb[ks][1] = 0u;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[ks][i] = 0.f;
+    }
+    m_a = m_b = l_a = l_b = 0.f;
   }
 
   // MQ: tok0 (first token of the tile), ctx, G and Q give the causal limits.
@@ -1942,6 +1971,10 @@ __global__ void __launch_bounds__(32 * (kMaxGroupHeads + kProducers), 1)
         if (slot >= 0)
           arrive_and_merge<T, D, (QMODE > 0)>(p, me.seq, kv_head, me.r0, me.r1, (me.flags >> 4) & 1, lane,
                                               kSplit);
+        // Split-column kernels sit at the register cap: writing the state here
+        // (the next segment's begin_segment rewrites it anyway) frees its
+        // registers for the merge above.
+        if constexpr (QMODE == 2) cons.clear();
       }
       if (++st == NS) {
         st = 0;
